@@ -1,0 +1,59 @@
+"""Tree ancestry: the mask that decides which draft nodes a node may attend to.
+
+"Tech Radar: SGLang EAGLE-2", section 2 ("Dynamic Tree-Attention Verification"):
+candidate i attends to candidate j iff j is an ancestor of i or j = i.
+Section 5, item 1: for trees of at most 64 nodes that relation is packed into
+one 64-bit word per node, and "is j an ancestor of i" is a single AND of the
+word with (1 << j).
+
+The tree arrives as a parent array in topological order: parents[0] = -1
+(the root, i.e. the last verified token) and 0 <= parents[i] < i.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def validate_parents(parents) -> None:
+    p = [int(x) for x in parents]
+    if len(p) == 0 or p[0] != -1:
+        raise ValueError("parents[0] must be -1")
+    for i in range(1, len(p)):
+        if not (0 <= p[i] < i):
+            raise ValueError(f"parents[{i}] = {p[i]} is not in [0, {i})")
+
+
+def ancestors(parents, i: int) -> list[int]:
+    """Strict ancestors of node i, found by following parent pointers to the root."""
+    out = []
+    j = int(parents[i])
+    while j >= 0:
+        out.append(j)
+        j = int(parents[j])
+    return out
+
+
+def mask_matrix(parents) -> np.ndarray:
+    """Dense M[i][j] = 1 iff j in Ancestors(i) or j == i (section 2 of the radar page)."""
+    validate_parents(parents)
+    n = len(parents)
+    m = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        m[i, i] = True
+        for j in ancestors(parents, i):
+            m[i, j] = True
+    return m
+
+
+def ancestor_bitmasks(parents) -> list[int]:
+    """mask_i with bit j set iff M[i][j] (section 5 item 1 of the radar page); N <= 64."""
+    m = mask_matrix(parents)
+    n = len(parents)
+    if n > 64:
+        raise ValueError("a 64-bit ancestry mask holds at most 64 nodes")
+    return [sum(1 << j for j in range(n) if m[i, j]) for i in range(n)]
+
+
+def children(parents, i: int) -> list[int]:
+    """Children of node i in ascending node index (the order the walk tries them)."""
+    return [c for c in range(1, len(parents)) if int(parents[c]) == i]
