@@ -1,0 +1,407 @@
+"""Benchmark of the tree-verify step: one tree_attn_verify (one layer) + one tree_accept.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  Inputs are seeded synthetic stand-ins with the
+workload's shapes; they are built once and stay resident in HBM for `value`.
+`e2e` repeats the step through the same C-ABI calls with every per-step input
+copied in from pinned host memory and the results copied back.  The reference
+arm times the float64 CPU oracle on a bounded sample of the same workload.
+Multi-GPU runs (torchrun) are independent replicas: weak scaling, no collective
+on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+from gen import inputs as gi  # noqa: E402
+
+METRIC = "tree-verify steps/s & KV-read HBM GB/s (frac of peak) per batch×prefix×tree"
+DEFAULT_WORKLOAD = "c4_llama3_70b_bf16_t0.7"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def algorithmic_work(x: gi.TreeInputs):
+    """Bytes and FLOPs one tree_attn_verify must move / do, and the accept bytes."""
+    w = x.workload
+    eb = 2 if w.dtype == "bf16" else 4
+    ntok = x.prefix_lens.astype(np.int64) + w.num_nodes
+    kv_bytes = int(ntok.sum()) * w.num_kv_heads * w.head_dim * 2 * eb
+    qo_bytes = 2 * w.batch * w.num_nodes * w.num_q_heads * w.head_dim * eb
+    pt_bytes = int(((ntok + w.page_size - 1) // w.page_size).sum()) * 4
+    attn_bytes = kv_bytes + qo_bytes + pt_bytes
+    attn_flops = 4 * w.num_q_heads * w.head_dim * int((w.num_nodes * ntok).sum())
+    rows = w.batch * w.num_nodes * w.vocab * 4
+    accept_bytes = rows * (1 if w.greedy else 2)
+    return dict(kv_bytes=kv_bytes, attn_bytes=attn_bytes, attn_flops=attn_flops, accept_bytes=accept_bytes)
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "eagle_speculative_tree_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("attn_") or f in ("common.cuh", "tree_mask.cu"):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        recs = json.load(f)
+    for r in recs:
+        if r.get("workload") == workload and r.get("kernel") == kernel and \
+                r.get("source_digest") == kernel_source_digest():
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import eagle_speculative_tree_gb300 as ts
+
+    w = gen.get(args.workload)
+    x = gi.make_inputs(w)
+    bf = w.dtype == "bf16"
+
+    def t(a, bf16=False, pin=False):
+        a = np.ascontiguousarray(a)
+        h = torch.from_numpy(a.view(np.int16) if bf16 else a)
+        h = h.pin_memory() if pin else h.to(dev)
+        return h.view(torch.bfloat16) if bf16 else h
+
+    d = dict(q=t(x.q, bf), k=t(x.k_pages, bf), v=t(x.v_pages, bf), pt=t(x.page_table), pl=t(x.prefix_lens),
+             par=t(x.tree_parents), lg=t(x.target_logits), tok=t(x.draft_tokens),
+             qp=None if w.greedy else t(x.draft_probs), u=None if w.greedy else t(x.uniforms))
+    out = torch.empty_like(d["q"])
+    prob = ts.attn_problem(d["q"], d["k"], d["pt"])
+    plan = ts.attn_plan(prob)
+    ws_a = torch.empty(ts.attn_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(ts.accept_workspace_bytes(w.batch, w.num_nodes, w.vocab), dtype=torch.uint8, device=dev)
+    path = torch.empty((w.batch, w.num_nodes), dtype=torch.int32, device=dev)
+    alen = torch.empty((w.batch,), dtype=torch.int32, device=dev)
+    bonus = torch.empty((w.batch,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(inp):
+        ts.tree_attn_verify(inp["q"], d["k"], d["v"], inp["pt"], inp["pl"], inp["par"], out,
+                            workspace=ws_a, stream=stream)
+        ts.tree_accept(inp["lg"], inp["tok"], inp["qp"], inp["par"], inp["u"], w.temperature,
+                       accept_path=path, accept_len=alen, bonus_token=bonus, workspace=ws_b, stream=stream)
+
+    resident = dict(q=d["q"], pt=d["pt"], pl=d["pl"], par=d["par"], lg=d["lg"], tok=d["tok"], qp=d["qp"],
+                    u=d["u"])
+    for _ in range(args.warmup):
+        step(resident)
+    torch.cuda.synchronize()
+    if ts.read_status(ws_a) or ts.read_status(ws_b):
+        raise RuntimeError("device status flagged an input error")
+
+    # ---- device-resident timed region
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    n0 = ts.launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        ts.tree_attn_verify(resident["q"], d["k"], d["v"], resident["pt"], resident["pl"], resident["par"], out,
+                            workspace=ws_a, stream=stream)
+        ev[i][1].record(stream)
+        ts.tree_accept(resident["lg"], resident["tok"], resident["qp"], resident["par"], resident["u"],
+                       w.temperature, accept_path=path, accept_len=alen, bonus_token=bonus, workspace=ws_b,
+                       stream=stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = ts.launch_count() - n0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    t_attn = float(np.mean(attn_ms))
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # ---- end to end: per-step inputs from pinned host memory, results back to the host
+    host = dict(q=t(x.q, bf, pin=True), pt=t(x.page_table, pin=True), pl=t(x.prefix_lens, pin=True),
+                par=t(x.tree_parents, pin=True), lg=t(x.target_logits, pin=True), tok=t(x.draft_tokens, pin=True),
+                qp=None if w.greedy else t(x.draft_probs, pin=True), u=None if w.greedy else t(x.uniforms, pin=True))
+    dst = dict(q=torch.empty_like(d["q"]), pt=torch.empty_like(d["pt"]), pl=torch.empty_like(d["pl"]),
+               par=torch.empty_like(d["par"]), lg=torch.empty_like(d["lg"]), tok=torch.empty_like(d["tok"]),
+               qp=None if w.greedy else torch.empty_like(d["qp"]), u=None if w.greedy else torch.empty_like(d["u"]))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    path_h = torch.empty(path.shape, dtype=path.dtype).pin_memory()
+    alen_h = torch.empty(alen.shape, dtype=alen.dtype).pin_memory()
+    bonus_h = torch.empty(bonus.shape, dtype=bonus.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in (out_h, path_h, alen_h, bonus_h))
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                dst[k].copy_(v, non_blocking=True)
+        step(dst)
+        out_h.copy_(out, non_blocking=True)
+        path_h.copy_(path, non_blocking=True)
+        alen_h.copy_(alen, non_blocking=True)
+        bonus_h.copy_(bonus, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    K2 = max(3, min(K, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K2
+
+    # ---- report
+    work = algorithmic_work(x)
+    hbm, tf_burst, tf_sus, src = peaks()
+    kv_gbs = work["kv_bytes"] / (t_attn * 1e-3) / 1e9
+    attn_gbs = work["attn_bytes"] / (t_attn * 1e-3) / 1e9
+    attn_tflops = work["attn_flops"] / (t_attn * 1e-3) / 1e12
+    t_hbm = work["attn_bytes"] / (hbm * 1e9)
+    t_tc = work["attn_flops"] / (tf_sus * 1e12)
+    kernel_name = "attn_simt_kernel" if plan.kernel == 1 else "attn_tc_kernel"
+    traffic = recorded_traffic(w.name, kernel_name)
+    if t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": tf_sus, "unit": "TFLOP/s",
+                "frac": round(attn_tflops / tf_sus, 4), "traffic": traffic}
+    else:
+        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(attn_gbs / hbm, 4), "traffic": traffic}
+    roof.update({"kernel": f"tree_attn_verify ({kernel_name} + prologue" + (" + merge)" if plan.merge else ")"),
+                 "peak_source": src, "algorithmic_bytes": work["attn_bytes"], "algorithmic_flops": work["attn_flops"],
+                 "launch_ms": round(t_attn, 4)})
+    ms_step = total_ms / K
+    lens = alen.cpu().numpy()
+    line = {
+        "metric": METRIC, "value": round(world * K / (total_ms * 1e-3), 2), "unit": "steps/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; shapes and distributions of the workload, no model weights)",
+        "config": {"workload": w.name, "batch": w.batch, "prefix": [w.prefix_lo, w.prefix_hi],
+                   "tree_nodes": w.num_nodes, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "page_size": w.page_size, "vocab": w.vocab,
+                   "temperature": w.temperature, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 (KV {work['kv_bytes'] / 1e9:.2f} GB, accept rows "
+                         f"{work['accept_bytes'] / 1e9:.2f} GB per step)"},
+        "kv_read_gbs": round(kv_gbs, 1), "kv_frac_of_hbm_peak": round(kv_gbs / hbm, 4),
+        "t_attn_ms": round(t_attn, 4), "t_accept_ms": round(ms_step - t_attn, 4),
+        "attn_plan": {"kernel": kernel_name, "num_splits": plan.num_splits, "split_tokens": plan.split_tokens,
+                      "merge": bool(plan.merge)},
+        "mean_accept_len": round(float(lens.mean()), 3), "tokens_per_step": round(float(lens.mean()) + 1, 3),
+        "roofline": roof,
+        "e2e": {"value": round(world / (e2e_ms * 1e-3), 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+class OracleSample:
+    """The float64 oracle on a bounded sample of a workload, scaled to one full step."""
+
+    def __init__(self, w):
+        from oracle import accept as oacc
+        from oracle import attention as oatt
+        self.oacc, self.oatt, self.w = oacc, oatt, w
+        self.sample_b = min(2, w.batch)
+        self.x = gi.make_inputs(w.with_batch(self.sample_b))
+        dt = w.dtype
+        self.q, self.kp, self.vp = gi.as_float(self.x.q, dt), gi.as_float(self.x.k_pages, dt), \
+            gi.as_float(self.x.v_pages, dt)
+        full_prefix = gi.make_inputs(w, with_accept=False, with_attention=False).prefix_lens.astype(np.int64)
+        self.full_tok = int((full_prefix + w.num_nodes).sum()) * w.num_kv_heads
+        self.pairs = [(b, h) for b in range(self.sample_b) for h in range(w.num_kv_heads)]
+
+    def run(self, budget_s: float):
+        w, x = self.w, self.x
+        done, t_att = [], 0.0
+        for pr in self.pairs:
+            t0 = time.perf_counter()
+            self.oatt.tree_attention(self.q, self.kp, self.vp, x.page_table, x.prefix_lens, x.tree_parents,
+                                     w.page_size, [pr])
+            t_att += time.perf_counter() - t0
+            done.append(pr)
+            if t_att > budget_s * 0.8:
+                break
+        t0 = time.perf_counter()
+        self.oacc.tree_accept(x.target_logits, x.draft_tokens, x.draft_probs, x.tree_parents, x.uniforms,
+                              w.temperature)
+        t_acc = time.perf_counter() - t0
+        samp_tok = sum(int(x.prefix_lens[b]) + w.num_nodes for b, _ in done)
+        t_attn_full = t_att * self.full_tok / samp_tok
+        t_acc_full = t_acc * w.batch / self.sample_b
+        t_step = t_attn_full + t_acc_full
+        return {"value": round(1.0 / t_step, 6), "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"float64 oracle: attention over {len(done)} (sequence, kv head) pairs and the accept "
+                          f"walk over {self.sample_b} sequences, scaled by tokens to the full {w.name} step",
+                "t_attn_s_full_step": round(t_attn_full, 3), "t_accept_s_full_step": round(t_acc_full, 3)}
+
+
+def cpu_baseline(w, budget_s: float = 20.0):
+    return OracleSample(w).run(budget_s)
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    w = gen.get(args.workload)
+    sampler = OracleSample(w)
+    budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    per = []
+    for i in range(args.warmup + args.steps):
+        cb = sampler.run(budget)
+        if i >= args.warmup:
+            per.append(cb)
+    value = float(np.mean([c["value"] for c in per]))
+    cb = dict(per[-1])
+    cb["value"] = round(value, 6)
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "steps/s", "impl": "reference",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000.0 / value, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "batch": w.batch, "prefix": [w.prefix_lo, w.prefix_hi],
+                       "tree_nodes": w.num_nodes, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "vocab": w.vocab, "temperature": w.temperature},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS) +
+                    [f"{n}@b{b}" for n in gen.WORKLOADS for b in (1, 2, 8, 16, 32, 64)])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,228 @@
+"""Python binding of libtreespec (tree-attention verify + accept walk on GB300).
+
+Argument marshalling only: every step runs in the CUDA library.  torch tensors
+carry device memory and streams; nothing here computes any part of the method.
+Importing the package fails if the compiled library is missing -- build it with
+`python -m eagle_speculative_tree_gb300.build` (or `__graft_entry__.build()`).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtreespec.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "treespec.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libtreespec.so is not built ({LIB_PATH}); run eagle_speculative_tree_gb300/build.py")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+DTYPE_F32, DTYPE_BF16 = 0, 1
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC = 0, 1, 2
+STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT"}
+
+
+class AttnShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_nodes", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
+        "max_pages_per_seq", "num_pool_pages", "dtype", "kernel", "num_splits")]
+
+
+class AttnPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "kernel", "num_splits", "split_tokens", "rows_per_block", "row_blocks", "merge")]
+
+
+_vp, _i32p, _f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_lib.treespec_attn_workspace_bytes.argtypes = [ctypes.POINTER(AttnShape)]
+_lib.treespec_attn_workspace_bytes.restype = ctypes.c_size_t
+_lib.treespec_attn_plan_for.argtypes = [ctypes.POINTER(AttnShape), ctypes.POINTER(AttnPlan)]
+_lib.treespec_attn_plan_for.restype = ctypes.c_int
+_lib.tree_attn_verify.argtypes = [_vp] * 7 + [ctypes.POINTER(AttnShape), _vp, ctypes.c_size_t, _vp]
+_lib.tree_attn_verify.restype = ctypes.c_int
+_lib.treespec_accept_workspace_bytes.argtypes = [ctypes.c_int32] * 3
+_lib.treespec_accept_workspace_bytes.restype = ctypes.c_size_t
+_lib.tree_accept.argtypes = [_vp] * 5 + [ctypes.c_float] + [_vp] * 3 + [ctypes.c_int32] * 3 + \
+    [_vp, ctypes.c_size_t, _vp]
+_lib.tree_accept.restype = ctypes.c_int
+_lib.treespec_read_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
+_lib.treespec_read_status.restype = ctypes.c_int
+_lib.treespec_error_string.argtypes = [ctypes.c_int]
+_lib.treespec_error_string.restype = ctypes.c_char_p
+_lib.treespec_version.restype = ctypes.c_int
+_lib.treespec_launch_count.restype = ctypes.c_uint64
+
+
+class TreespecError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(f"treespec error {code}: {_lib.treespec_error_string(code).decode()}")
+
+
+def _check(code: int) -> None:
+    if code != 0:
+        raise TreespecError(code)
+
+
+def exported_symbols() -> list[str]:
+    """Function names declared in include/treespec.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def version() -> int:
+    return _lib.treespec_version()
+
+
+def launch_count() -> int:
+    return int(_lib.treespec_launch_count())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device) -> None:
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+@dataclass
+class AttnProblem:
+    batch: int
+    num_nodes: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    max_pages_per_seq: int
+    num_pool_pages: int
+    dtype: int
+    kernel: int = KERNEL_AUTO
+    num_splits: int = 0
+
+    def c_shape(self) -> AttnShape:
+        return AttnShape(self.batch, self.num_nodes, self.num_q_heads, self.num_kv_heads, self.head_dim,
+                         self.page_size, self.max_pages_per_seq, self.num_pool_pages, self.dtype,
+                         self.kernel, self.num_splits)
+
+
+def attn_problem(q: torch.Tensor, k_pages: torch.Tensor, page_table: torch.Tensor, *,
+                 kernel: int = KERNEL_AUTO, num_splits: int = 0) -> AttnProblem:
+    B, N, Hq, D = q.shape
+    P, ps, Hkv, D2 = k_pages.shape
+    if D2 != D:
+        raise ValueError("head_dim of q and k_pages differ")
+    dt = DTYPE_BF16 if q.dtype == torch.bfloat16 else DTYPE_F32
+    return AttnProblem(B, N, Hq, Hkv, D, ps, page_table.shape[1], P, dt, kernel, num_splits)
+
+
+def attn_workspace_bytes(prob: AttnProblem) -> int:
+    n = _lib.treespec_attn_workspace_bytes(ctypes.byref(prob.c_shape()))
+    if n == 0:
+        raise ValueError(f"unsupported attention shape {prob}")
+    return int(n)
+
+
+def attn_plan(prob: AttnProblem) -> AttnPlan:
+    plan = AttnPlan()
+    _check(_lib.treespec_attn_plan_for(ctypes.byref(prob.c_shape()), ctypes.byref(plan)))
+    return plan
+
+
+def tree_attn_verify(q, k_pages, v_pages, page_table, prefix_lens, tree_parents, out=None, *,
+                     kernel: int = KERNEL_AUTO, num_splits: int = 0,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Tree-attention verification pass; see include/treespec.h for the operation.
+
+    q [B][N][Hq][D], k_pages / v_pages [P][16][Hkv][D] (float32 or bfloat16),
+    page_table [B][max_pages] int32, prefix_lens [B] int32, tree_parents [B][N] int32.
+    Returns out [B][N][Hq][D] in q's dtype.
+    """
+    dev = q.device
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
+    _need(q, "q", dt, dev)
+    _need(k_pages, "k_pages", dt, dev)
+    _need(v_pages, "v_pages", dt, dev)
+    _need(page_table, "page_table", torch.int32, dev)
+    _need(prefix_lens, "prefix_lens", torch.int32, dev)
+    _need(tree_parents, "tree_parents", torch.int32, dev)
+    prob = attn_problem(q, k_pages, page_table, kernel=kernel, num_splits=num_splits)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dt, dev)
+    need = attn_workspace_bytes(prob)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(_lib.tree_attn_verify(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(prefix_lens), _ptr(tree_parents),
+        _ptr(out), ctypes.byref(prob.c_shape()), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream, dev)))
+    return out
+
+
+def accept_workspace_bytes(batch: int, num_nodes: int, vocab: int) -> int:
+    n = _lib.treespec_accept_workspace_bytes(batch, num_nodes, vocab)
+    if n == 0:
+        raise ValueError("unsupported accept sizes")
+    return int(n)
+
+
+def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms, temperature: float, *,
+                accept_path=None, accept_len=None, bonus_token=None,
+                workspace: Optional[torch.Tensor] = None, stream=None):
+    """Accept walk; see include/treespec.h.  Returns (accept_path, accept_len, bonus_token)."""
+    dev = target_logits.device
+    B, N, V = target_logits.shape
+    _need(target_logits, "target_logits", torch.float32, dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, dev)
+    _need(tree_parents, "tree_parents", torch.int32, dev)
+    if temperature > 0:
+        _need(draft_probs, "draft_probs", torch.float32, dev)
+        _need(uniforms, "uniforms", torch.float32, dev)
+    if accept_path is None:
+        accept_path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if accept_len is None:
+        accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if bonus_token is None:
+        bonus_token = torch.empty((B,), dtype=torch.int32, device=dev)
+    need = accept_workspace_bytes(B, N, V)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(_lib.tree_accept(
+        _ptr(target_logits), _ptr(draft_tokens), _ptr(draft_probs) if temperature > 0 else None,
+        _ptr(tree_parents), _ptr(uniforms) if temperature > 0 else None, float(temperature),
+        _ptr(accept_path), _ptr(accept_len), _ptr(bonus_token), B, N, V,
+        _ptr(workspace), workspace.numel(), _stream_handle(stream, dev)))
+    return accept_path, accept_len, bonus_token
+
+
+def read_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the device status word of the last call that used `workspace`."""
+    st = ctypes.c_uint32(0)
+    _check(_lib.treespec_read_status(_ptr(workspace), ctypes.byref(st),
+                                     _stream_handle(stream, workspace.device)))
+    return int(st.value)
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded C library (for callers that pass raw pointers)."""
+    return _lib

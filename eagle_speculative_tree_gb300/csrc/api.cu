@@ -1,0 +1,310 @@
+// Host side of libtreespec: argument checks, the split planner, workspace layout and
+// launches.  Every exported symbol is declared in include/treespec.h.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace treespec {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kDefaultSms = 152;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+// Per-device attributes, read once.  Returns false when no device is usable.
+bool device_info(DeviceInfo* out) {
+    static DeviceInfo cache[kMaxDevices];
+    static std::mutex mu;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms == 0) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        cache[dev] = d;
+    }
+    *out = cache[dev];
+    return true;
+}
+
+int sm_count_or_default() {
+    DeviceInfo d;
+    return device_info(&d) ? d.sms : kDefaultSms;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_attn_shape(const treespec_attn_shape* s) {
+    if (!s) return TREESPEC_ERR_NULL_POINTER;
+    if (s->dtype != TREESPEC_DTYPE_F32 && s->dtype != TREESPEC_DTYPE_BF16) return TREESPEC_ERR_DTYPE;
+    if (s->batch < 1 || s->batch > 65535) return TREESPEC_ERR_SHAPE;
+    if (s->num_nodes < 1 || s->num_nodes > kMaxNodes) return TREESPEC_ERR_SHAPE;
+    if (s->num_kv_heads < 1 || s->num_q_heads < 1 || s->num_q_heads % s->num_kv_heads) return TREESPEC_ERR_SHAPE;
+    if (s->head_dim != 64 && s->head_dim != 128) return TREESPEC_ERR_SHAPE;
+    if (s->page_size != 16) return TREESPEC_ERR_SHAPE;
+    if (s->max_pages_per_seq < 1 || s->num_pool_pages < 1) return TREESPEC_ERR_SHAPE;
+    if ((long long)s->max_pages_per_seq * s->page_size > (1ll << 30)) return TREESPEC_ERR_SHAPE;
+    const long long R = (long long)s->num_nodes * (s->num_q_heads / s->num_kv_heads);
+    if (R > 4096 || (long long)s->num_kv_heads * ((R + 63) / 64) > 65535) return TREESPEC_ERR_SHAPE;
+    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC) return TREESPEC_ERR_SHAPE;
+    if (s->num_splits < 0) return TREESPEC_ERR_SHAPE;
+    if (s->kernel == TREESPEC_KERNEL_TC) return TREESPEC_ERR_DTYPE;   // not built in this library yet
+    return TREESPEC_OK;
+}
+
+AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
+    AttnPlan p{};
+    const int G = s.num_q_heads / s.num_kv_heads;
+    const int R = s.num_nodes * G;
+    p.kernel = TREESPEC_KERNEL_SIMT;
+    p.rows_per_block = R < 64 ? R : 64;
+    p.row_blocks = (R + p.rows_per_block - 1) / p.rows_per_block;
+    const long long max_tokens = (long long)s.max_pages_per_seq * s.page_size;
+    const int tile = 128;                       // split sizes are multiples of every tile size
+    int splits;
+    if (s.num_splits > 0) {
+        splits = s.num_splits;
+    } else {
+        const long long units = (long long)s.batch * s.num_kv_heads * p.row_blocks;
+        const long long target = 2ll * sms;      // two waves of CTAs, then merge
+        splits = int((target + units - 1) / units);
+        if (splits < 1) splits = 1;
+    }
+    long long chunk = (max_tokens + splits - 1) / splits;
+    chunk = (chunk + tile - 1) / tile * tile;
+    if (s.num_splits == 0 && chunk > 4096) chunk = 4096;     // bounded CTA length (ragged batches)
+    if (chunk < tile) chunk = tile;
+    p.split_tokens = int(chunk);
+    p.num_splits = int((max_tokens + chunk - 1) / chunk);
+    if (p.num_splits > 65535) {
+        p.num_splits = 65535;
+        p.split_tokens = int((max_tokens + 65534) / 65535);
+        p.split_tokens = (p.split_tokens + tile - 1) / tile * tile;
+    }
+    p.merge = p.num_splits > 1;
+    return p;
+}
+
+AttnLayout attn_layout(const treespec_attn_shape& s, const AttnPlan& p) {
+    AttnLayout L{};
+    const size_t R = size_t(s.num_nodes) * (s.num_q_heads / s.num_kv_heads);
+    size_t off = 0;
+    L.status = off;
+    off += kWsAlign;
+    L.anc = off;
+    off = align_up(off + size_t(s.batch) * s.num_nodes * 8, kWsAlign);
+    L.lens = off;
+    off = align_up(off + size_t(s.batch) * 4, kWsAlign);
+    const size_t parts = p.merge ? size_t(s.batch) * s.num_kv_heads * p.num_splits * R : 0;
+    L.ml = off;
+    off = align_up(off + parts * 2 * 4, kWsAlign);
+    L.acc = off;
+    off = align_up(off + parts * s.head_dim * 4, kWsAlign);
+    L.total = off;
+    return L;
+}
+
+AcceptLayout accept_layout(int B, int N) {
+    AcceptLayout L{};
+    size_t off = 0;
+    L.status = off;
+    off += kWsAlign;
+    L.amax = off;
+    off = align_up(off + size_t(B) * N * 4, kWsAlign);
+    L.stats = off;
+    off = align_up(off + size_t(B) * N * 8, kWsAlign);
+    L.zs = off;
+    off = align_up(off + size_t(B) * N * kMaxNodes * 4, kWsAlign);
+    L.total = off;
+    return L;
+}
+
+int check_device() {
+    DeviceInfo d;
+    if (!device_info(&d)) return TREESPEC_ERR_DEVICE;
+    if (d.cc_major != 10 || d.cc_minor != 3) return TREESPEC_ERR_DEVICE;
+    return TREESPEC_OK;
+}
+
+}  // namespace
+}  // namespace treespec
+
+using namespace treespec;
+
+extern "C" size_t treespec_attn_workspace_bytes(const treespec_attn_shape* shape) {
+    if (check_attn_shape(shape) != TREESPEC_OK) return 0;
+    return attn_layout(*shape, make_plan(*shape, sm_count_or_default())).total;
+}
+
+extern "C" int treespec_attn_plan_for(const treespec_attn_shape* shape, treespec_attn_plan* plan) {
+    const int rc = check_attn_shape(shape);
+    if (rc != TREESPEC_OK) return rc;
+    if (!plan) return TREESPEC_ERR_NULL_POINTER;
+    const AttnPlan p = make_plan(*shape, sm_count_or_default());
+    plan->kernel = p.kernel;
+    plan->num_splits = p.num_splits;
+    plan->split_tokens = p.split_tokens;
+    plan->rows_per_block = p.rows_per_block;
+    plan->row_blocks = p.row_blocks;
+    plan->merge = p.merge;
+    return TREESPEC_OK;
+}
+
+extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* page_table, const int32_t* prefix_lens,
+                                const int32_t* tree_parents, void* out,
+                                const treespec_attn_shape* shape, void* workspace,
+                                size_t workspace_bytes, treespec_stream_t stream) {
+    int rc = check_attn_shape(shape);
+    if (rc != TREESPEC_OK) return rc;
+    if (!q || !k_pages || !v_pages || !page_table || !prefix_lens || !tree_parents || !out)
+        return TREESPEC_ERR_NULL_POINTER;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+        return TREESPEC_ERR_ALIGNMENT;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)) return TREESPEC_ERR_WORKSPACE;
+    rc = check_device();
+    if (rc != TREESPEC_OK) return rc;
+    const treespec_attn_shape& s = *shape;
+    const AttnPlan plan = make_plan(s, sm_count_or_default());
+    const AttnLayout lay = attn_layout(s, plan);
+    if (workspace_bytes < lay.total) return TREESPEC_ERR_WORKSPACE;
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    AttnParams p{};
+    p.q = q;
+    p.k = k_pages;
+    p.v = v_pages;
+    p.page_table = page_table;
+    p.prefix_lens = prefix_lens;
+    p.parents = tree_parents;
+    p.out = out;
+    p.status = reinterpret_cast<uint32_t*>(ws + lay.status);
+    p.anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
+    p.lens = reinterpret_cast<int32_t*>(ws + lay.lens);
+    p.part_ml = reinterpret_cast<float*>(ws + lay.ml);
+    p.part_acc = reinterpret_cast<float*>(ws + lay.acc);
+    p.B = s.batch;
+    p.N = s.num_nodes;
+    p.Hq = s.num_q_heads;
+    p.Hkv = s.num_kv_heads;
+    p.G = s.num_q_heads / s.num_kv_heads;
+    p.R = p.N * p.G;
+    p.D = s.head_dim;
+    p.ps = s.page_size;
+    p.max_pages = s.max_pages_per_seq;
+    p.num_pool_pages = s.num_pool_pages;
+    p.num_splits = plan.num_splits;
+    p.split_tokens = plan.split_tokens;
+    p.rows_per_block = plan.rows_per_block;
+    p.row_blocks = plan.row_blocks;
+    p.merge = plan.merge;
+    p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(s.head_dim)));
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (launch_tree_prologue(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches++;
+    if (launch_attn_simt(p, s.dtype, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches++;
+    if (plan.merge) {
+        if (launch_attn_merge(p, s.dtype, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+        g_launches++;
+    }
+    return TREESPEC_OK;
+}
+
+extern "C" size_t treespec_accept_workspace_bytes(int32_t batch, int32_t num_nodes, int32_t vocab) {
+    if (batch < 1 || num_nodes < 1 || num_nodes > kMaxNodes || vocab < 1 || vocab > (1 << 30)) return 0;
+    return accept_layout(batch, num_nodes).total;
+}
+
+extern "C" int tree_accept(const float* target_logits, const int32_t* draft_tokens,
+                           const float* draft_probs, const int32_t* tree_parents,
+                           const float* uniforms, float temperature, int32_t* accept_path,
+                           int32_t* accept_len, int32_t* bonus_token, int32_t batch,
+                           int32_t num_nodes, int32_t vocab, void* workspace,
+                           size_t workspace_bytes, treespec_stream_t stream) {
+    if (batch < 1 || num_nodes < 1 || num_nodes > kMaxNodes || vocab < 1 || vocab > (1 << 30))
+        return TREESPEC_ERR_SHAPE;
+    if ((long long)batch * num_nodes > 0x7fffffffll) return TREESPEC_ERR_SHAPE;
+    if (!target_logits || !draft_tokens || !tree_parents || !accept_path || !accept_len || !bonus_token)
+        return TREESPEC_ERR_NULL_POINTER;
+    if (!(temperature >= 0.f) || std::isinf(temperature)) return TREESPEC_ERR_SAMPLING;
+    const bool stoch = temperature > 0.f;
+    if (stoch && (!draft_probs || !uniforms)) return TREESPEC_ERR_SAMPLING;
+    if (!aligned16(target_logits) || (stoch && !aligned16(draft_probs))) return TREESPEC_ERR_ALIGNMENT;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)) return TREESPEC_ERR_WORKSPACE;
+    const AcceptLayout lay = accept_layout(batch, num_nodes);
+    if (workspace_bytes < lay.total) return TREESPEC_ERR_WORKSPACE;
+    const int rc = check_device();
+    if (rc != TREESPEC_OK) return rc;
+
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    AcceptParams p{};
+    p.logits = target_logits;
+    p.tokens = draft_tokens;
+    p.probs = draft_probs;
+    p.parents = tree_parents;
+    p.uniforms = uniforms;
+    p.path = accept_path;
+    p.len = accept_len;
+    p.bonus = bonus_token;
+    p.status = reinterpret_cast<uint32_t*>(ws + lay.status);
+    p.amax = reinterpret_cast<int32_t*>(ws + lay.amax);
+    p.stats = reinterpret_cast<float*>(ws + lay.stats);
+    p.zs = reinterpret_cast<float*>(ws + lay.zs);
+    p.B = batch;
+    p.N = num_nodes;
+    p.V = vocab;
+    p.temperature = temperature;
+    p.inv_t = stoch ? 1.f / temperature : 0.f;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (launch_accept(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches += 2;
+    return TREESPEC_OK;
+}
+
+extern "C" int treespec_read_status(const void* workspace, uint32_t* status, treespec_stream_t stream) {
+    if (!workspace || !status) return TREESPEC_ERR_NULL_POINTER;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (cudaMemcpy(status, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TREESPEC_ERR_LAUNCH;
+    return TREESPEC_OK;
+}
+
+extern "C" const char* treespec_error_string(int code) {
+    switch (code) {
+        case TREESPEC_OK: return "ok";
+        case TREESPEC_ERR_NULL_POINTER: return "a required pointer is NULL";
+        case TREESPEC_ERR_SHAPE: return "a size is outside the supported range";
+        case TREESPEC_ERR_DTYPE: return "unsupported dtype or kernel for this dtype";
+        case TREESPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case TREESPEC_ERR_SAMPLING: return "invalid temperature, or sampling inputs missing";
+        case TREESPEC_ERR_ALIGNMENT: return "a tensor is not 16-byte aligned";
+        case TREESPEC_ERR_DEVICE: return "no usable sm_103 CUDA device";
+        case TREESPEC_ERR_LAUNCH: return "the CUDA runtime rejected a launch";
+        default: return "unknown error code";
+    }
+}
+
+extern "C" int treespec_version(void) { return 100; }
+
+extern "C" uint64_t treespec_launch_count(void) { return g_launches.load(); }

@@ -1,0 +1,108 @@
+// Shared device helpers and launch parameter blocks of libtreespec.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "treespec.h"
+
+namespace treespec {
+
+constexpr int kMaxNodes = 64;          // one 64-bit ancestry word per node
+constexpr size_t kWsAlign = 256;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// bf16 <-> f32 on raw bit patterns (bf16 is the high half of an f32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return uint16_t((u >> 16) | 0x40u);   // NaN stays NaN
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return uint16_t(u >> 16);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ attention
+
+// Workspace of tree_attn_verify (offsets in bytes from the workspace base).
+struct AttnLayout {
+    size_t status, anc, lens, ml, acc, total;
+};
+
+struct AttnPlan {
+    int kernel;          // TREESPEC_KERNEL_SIMT / _TC
+    int num_splits;
+    int split_tokens;
+    int rows_per_block;
+    int row_blocks;
+    int merge;
+};
+
+struct AttnParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* page_table;
+    const int32_t* prefix_lens;   // caller's array (read by the prologue only)
+    const int32_t* parents;       // caller's array (read by the prologue only)
+    void* out;
+    uint32_t* status;
+    uint64_t* anc;                // [B][N] ancestor-or-self words
+    int32_t* lens;                // [B] validated prefix lengths, -1 = invalid sequence
+    float* part_ml;               // [B][Hkv][splits][R][2]  (m in log2 units, l)
+    float* part_acc;              // [B][Hkv][splits][R][D]
+    int B, N, Hq, Hkv, G, R, D, ps, max_pages, num_pool_pages;
+    int num_splits, split_tokens, rows_per_block, row_blocks, merge;
+    float scale_log2;             // log2(e) / sqrt(D)
+};
+
+// ------------------------------------------------------------------ accept
+
+struct AcceptLayout {
+    size_t status, amax, stats, zs, total;
+};
+
+struct AcceptParams {
+    const float* logits;
+    const int32_t* tokens;
+    const float* probs;
+    const int32_t* parents;
+    const float* uniforms;
+    int32_t* path;
+    int32_t* len;
+    int32_t* bonus;
+    uint32_t* status;
+    int32_t* amax;    // [B][N]   lowest argmax of each target row
+    float* stats;     // [B][N][2] (M, S): max of logits/T and sum of exp(logits/T - M)
+    float* zs;        // [B][N][64] Z_1.. of the sibling residual chain of each row
+    int B, N, V;
+    float temperature;
+    float inv_t;
+};
+
+// Kernel launchers (each returns cudaGetLastError() of its launch).
+cudaError_t launch_tree_prologue(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
+size_t attn_simt_smem_bytes(int dtype, int D, int R_block);
+
+}  // namespace treespec

@@ -1,0 +1,201 @@
+/*
+ * treespec -- tree-attention verification and the accept walk of EAGLE-2-style
+ * speculative decoding, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (from the pages this library follows):
+ *   - "Tech Radar: SGLang EAGLE-2", section 2 (Dynamic Tree-Attention Verification):
+ *     each draft node attends only to its tree ancestors and itself, on top of the
+ *     cached prefix; section 5 item 1: for trees of at most 64 nodes the ancestor
+ *     relation is one 64-bit word per node, tested with a single AND.
+ *   - "Speculative Decoding in Production: EAGLE-3 Dynamic Trees", section
+ *     "Mathematical Proof of Lossless Speedup", steps 1-3: accept a draft token with
+ *     probability min(1, p/q), otherwise resample from the normalised max(0, p - q);
+ *     section "From Linear Sequences to Dynamic Draft Trees": when branch B1 is
+ *     rejected the next sibling B2 is tried.
+ *   - "EAGLE-2 & Lookahead Decoding", section 4: greedy verification keeps the longest
+ *     path whose tokens the target agrees with.
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer owned by the caller; the library never
+ *     allocates, frees or retains memory.  Scratch space is the caller's `workspace`
+ *     (device memory, 256-byte aligned, at least the size the matching *_workspace_bytes
+ *     query returns for the same arguments).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and are stream-ordered: inputs may be reused once the stream reaches
+ *     the call's end.
+ *   - Return value: TREESPEC_OK, or a negative TREESPEC_ERR_* code for an argument the
+ *     host can check (nothing is launched in that case).  Index data that lives on the
+ *     device (parent arrays, page ids, prefix lengths, tokens) is checked by the kernels:
+ *     a bad entry sets a TREESPEC_STATUS_* bit in the workspace status word, the
+ *     offending element is skipped (never dereferenced), and the caller reads the word
+ *     with treespec_read_status() after the call.
+ *   - Tree layout: tree_parents[b][0] = -1 is the root (the last verified token) and
+ *     0 <= tree_parents[b][i] < i for i >= 1 (topological order), N <= 64.
+ */
+#ifndef TREESPEC_H
+#define TREESPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *treespec_stream_t;   /* a cudaStream_t */
+
+enum treespec_dtype {
+    TREESPEC_DTYPE_F32 = 0,    /* IEEE float32 storage and arithmetic */
+    TREESPEC_DTYPE_BF16 = 1,   /* bfloat16 storage, float32 accumulation */
+};
+
+enum treespec_kernel {
+    TREESPEC_KERNEL_AUTO = 0,  /* tensor-core kernel when N*G >= 64 rows and bf16, else CUDA cores */
+    TREESPEC_KERNEL_SIMT = 1,  /* CUDA-core split-KV kernel (any dtype) */
+    TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128) */
+};
+
+enum treespec_error {
+    TREESPEC_OK = 0,
+    TREESPEC_ERR_NULL_POINTER = -1,   /* a required pointer is NULL */
+    TREESPEC_ERR_SHAPE = -2,          /* a size is out of the supported range */
+    TREESPEC_ERR_DTYPE = -3,          /* unknown dtype, or a kernel that does not take it */
+    TREESPEC_ERR_WORKSPACE = -4,      /* workspace NULL, misaligned or too small */
+    TREESPEC_ERR_SAMPLING = -5,       /* temperature < 0 / NaN, or T > 0 without probs/uniforms */
+    TREESPEC_ERR_ALIGNMENT = -6,      /* a tensor is not 16-byte aligned */
+    TREESPEC_ERR_DEVICE = -7,         /* no usable CUDA device, or not sm_103 */
+    TREESPEC_ERR_LAUNCH = -8,         /* the CUDA runtime refused a launch */
+};
+
+enum treespec_status_bits {
+    TREESPEC_STATUS_BAD_PARENT = 1u << 0,  /* parents[0] != -1 or parents[i] not in [0, i) */
+    TREESPEC_STATUS_BAD_PAGE = 1u << 1,    /* a page id outside [0, num_pool_pages) */
+    TREESPEC_STATUS_BAD_LENGTH = 1u << 2,  /* prefix_len < 0 or prefix_len + N > pages * page_size */
+    TREESPEC_STATUS_BAD_TOKEN = 1u << 3,   /* a draft token outside [0, vocab) */
+    TREESPEC_STATUS_TIMEOUT = 1u << 4,     /* a bounded wait inside a kernel ran out */
+};
+
+/* ------------------------------------------------------------------ tree attention */
+
+typedef struct {
+    int32_t batch;              /* B >= 1 */
+    int32_t num_nodes;          /* N, tree nodes including the root, 1..64 */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv, Hq % Hkv == 0; G = Hq / Hkv query heads share a kv head */
+    int32_t head_dim;           /* D: 64 or 128 */
+    int32_t page_size;          /* tokens per KV page: 16 */
+    int32_t max_pages_per_seq;  /* row length of page_table */
+    int32_t num_pool_pages;     /* P, pages in k_pages / v_pages */
+    int32_t dtype;              /* enum treespec_dtype, shared by q, k_pages, v_pages, out */
+    int32_t kernel;             /* enum treespec_kernel (0 = automatic) */
+    int32_t num_splits;         /* KV splits per (sequence, kv head); 0 = planner's choice */
+} treespec_attn_shape;
+
+typedef struct {
+    int32_t kernel;             /* the kernel the call will run (SIMT or TC) */
+    int32_t num_splits;         /* KV splits per (sequence, kv head, row block) */
+    int32_t split_tokens;       /* logical tokens per split (a multiple of the tile) */
+    int32_t rows_per_block;     /* query rows (node x group) one CTA holds */
+    int32_t row_blocks;         /* ceil(N*G / rows_per_block) */
+    int32_t merge;              /* 1 if a split-merge kernel runs after the split kernel */
+} treespec_attn_plan;
+
+/* Workspace bytes tree_attn_verify needs for `shape` (0 if the shape is invalid). */
+size_t treespec_attn_workspace_bytes(const treespec_attn_shape *shape);
+
+/* How tree_attn_verify will execute `shape` on the current device.  Returns an error code. */
+int treespec_attn_plan_for(const treespec_attn_shape *shape, treespec_attn_plan *plan);
+
+/*
+ * tree_attn_verify -- one tree-attention verification pass (one layer) for a batch.
+ *
+ * Operation ("Tech Radar: SGLang EAGLE-2", section 2 mask M and section 5 bitmask):
+ * for sequence b with prefix length S = prefix_lens[b], the N tree tokens occupy
+ * logical positions S .. S+N-1 in node order.  Logical token t lives in physical
+ * page page_table[b][t / page_size], slot t % page_size.  For node i and query head
+ * hq (kv head h = hq / G):
+ *     allowed(i) = {0 .. S-1} U {S + j : j is an ancestor of i, or j == i}
+ *     out[b][i][hq] = softmax_t( q[b][i][hq] . K[t][h] / sqrt(D) ) over allowed(i),
+ *                     applied to V[t][h].
+ *
+ *   q            [B][N][Hq][D]            dtype
+ *   k_pages      [P][page_size][Hkv][D]   dtype  (the tree's own K at positions S..S+N-1)
+ *   v_pages      [P][page_size][Hkv][D]   dtype
+ *   page_table   [B][max_pages_per_seq]   int32, entries >= ceil((S+N)/page_size) unused
+ *   prefix_lens  [B]                      int32, S >= 0 and S + N <= max_pages_per_seq*page_size
+ *   tree_parents [B][N]                   int32, see the tree layout above
+ *   out          [B][N][Hq][D]            dtype, written in full (zeros for a sequence
+ *                                         whose prefix length is invalid)
+ * Slots of a sequence's last page beyond S+N and pages outside the table are never
+ * read, so they may hold anything (NaN included).  bf16 outputs are rounded to
+ * nearest-even from float32.  All tensors must be 16-byte aligned and contiguous.
+ */
+int tree_attn_verify(const void *q, const void *k_pages, const void *v_pages,
+                     const int32_t *page_table, const int32_t *prefix_lens,
+                     const int32_t *tree_parents, void *out,
+                     const treespec_attn_shape *shape,
+                     void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
+/* --------------------------------------------------------------------- accept walk */
+
+/* Workspace bytes tree_accept needs (0 if the sizes are invalid). */
+size_t treespec_accept_workspace_bytes(int32_t batch, int32_t num_nodes, int32_t vocab);
+
+/*
+ * tree_accept -- walk each sequence's draft tree from the root and decide which
+ * draft tokens the target accepts, plus the bonus token that follows them.
+ *
+ * Children of a node are tried in ascending node index.
+ * Greedy (temperature == 0; "EAGLE-2 & Lookahead Decoding", section 4): a child is
+ *   accepted iff its token equals the argmax of the current node's target logits
+ *   (ties: lowest token id); the bonus token is the argmax at the last accepted node.
+ * Stochastic (temperature > 0; rejection rule of "Speculative Decoding in Production:
+ *   EAGLE-3 Dynamic Trees", section "Mathematical Proof of Lossless Speedup"): with
+ *   p = softmax(target_logits[cur] / T), q = draft_probs[cur] and r = p, child c with
+ *   token x is accepted iff r(x) > 0 and uniforms[c] * q(x) <= r(x); on rejection
+ *   r <- max(0, r - q) / sum(max(0, r - q)) (left unchanged if that sum is 0) and the
+ *   next sibling is tried.  With no child accepted, the bonus token is the smallest v
+ *   with sum_{w <= v} r(w) > uniforms[0] * sum_w r(w).
+ *
+ *   target_logits [B][N][V] float32  row i = target logits after node i's token
+ *   draft_tokens  [B][N]    int32    token of node i (entry 0, the root, is unused)
+ *   draft_probs   [B][N][V] float32  q_i, the draft distribution i's children were drawn
+ *                                    from (used as given); may be NULL when T == 0
+ *   tree_parents  [B][N]    int32
+ *   uniforms      [B][N]    float32  uniforms[b][c], c >= 1: accept coin of node c;
+ *                                    uniforms[b][0]: the bonus-sample coin; NULL when T == 0
+ *   temperature   0 for greedy, else > 0
+ *   accept_path   [B][N]    int32    out: accepted node indices root-first, root excluded,
+ *                                    padded with -1
+ *   accept_len    [B]       int32    out: number of accepted draft nodes
+ *   bonus_token   [B]       int32    out
+ * Limits: N in 1..64, V in 1..2^30.  A draft token outside [0, V) is rejected and
+ * flagged with TREESPEC_STATUS_BAD_TOKEN.
+ */
+int tree_accept(const float *target_logits, const int32_t *draft_tokens,
+                const float *draft_probs, const int32_t *tree_parents,
+                const float *uniforms, float temperature,
+                int32_t *accept_path, int32_t *accept_len, int32_t *bonus_token,
+                int32_t batch, int32_t num_nodes, int32_t vocab,
+                void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
+/* ------------------------------------------------------------------------- helpers */
+
+/* Synchronise `stream` and copy the status word of a workspace used by the last call
+ * on it into *status (0 = clean).  Returns an error code. */
+int treespec_read_status(const void *workspace, uint32_t *status, treespec_stream_t stream);
+
+/* Static description of an error code. */
+const char *treespec_error_string(int code);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int treespec_version(void);
+
+/* Kernels this process has launched through the library so far (all entry points). */
+uint64_t treespec_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREESPEC_H */

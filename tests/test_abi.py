@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad arguments on
+the host before any launch.  Runs without a GPU (fake device pointers are never
+dereferenced because every call below fails validation first)."""
+import ctypes
+import re
+
+import pytest
+
+import __graft_entry__
+
+__graft_entry__.build()
+import eagle_speculative_tree_gb300 as ts  # noqa: E402
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced
+
+
+def test_every_declared_symbol_is_exported():
+    names = ts.exported_symbols()
+    assert {"tree_attn_verify", "tree_accept", "treespec_attn_workspace_bytes",
+            "treespec_accept_workspace_bytes", "treespec_read_status"} <= set(names)
+    lib = ctypes.CDLL(ts.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_header_declarations_are_extern_c():
+    text = open(ts.HEADER_PATH).read()
+    assert re.search(r'extern "C"', text)
+
+
+def test_version_and_error_strings():
+    assert ts.version() >= 100
+    lib = ts.raw_library()
+    for code in range(-8, 1):
+        assert lib.treespec_error_string(code)
+
+
+def shape(**kw):
+    base = dict(batch=1, num_nodes=8, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                max_pages_per_seq=129, num_pool_pages=200, dtype=ts.DTYPE_BF16)
+    base.update(kw)
+    return ts.AttnProblem(**base)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(num_nodes=65), dict(num_nodes=0), dict(num_q_heads=30), dict(head_dim=96),
+    dict(page_size=32), dict(batch=0), dict(dtype=7), dict(max_pages_per_seq=0),
+    dict(num_splits=-1), dict(kernel=9),
+])
+def test_attention_rejects_bad_shapes(kw):
+    prob = shape(**kw)
+    assert ts.raw_library().treespec_attn_workspace_bytes(ctypes.byref(prob.c_shape())) == 0
+    rc = ts.raw_library().tree_attn_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                           ctypes.byref(prob.c_shape()), FAKE * 256, 1 << 30, None)
+    assert rc in (ts.TreespecError(-2).code, -3, -2)
+    assert rc < 0
+
+
+def test_attention_rejects_null_and_misaligned():
+    prob = shape()
+    lib = ts.raw_library()
+    assert lib.tree_attn_verify(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(prob.c_shape()),
+                                FAKE * 256, 1 << 30, None) == -1
+    assert lib.tree_attn_verify(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(prob.c_shape()),
+                                FAKE * 256, 1 << 30, None) == -6
+    assert lib.tree_attn_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(prob.c_shape()),
+                                FAKE + 16, 1 << 30, None) == -4
+
+
+def test_plan_and_workspace_query():
+    prob = shape()
+    plan = ts.attn_plan(prob)
+    assert plan.num_splits >= 1 and plan.split_tokens % 128 == 0
+    assert plan.num_splits * plan.split_tokens >= prob.max_pages_per_seq * 16
+    assert ts.attn_workspace_bytes(prob) > 0
+    single = ts.attn_plan(shape(num_splits=1))
+    assert single.num_splits == 1 and single.merge == 0
+
+
+def test_accept_rejects_bad_arguments():
+    lib = ts.raw_library()
+
+    def call(logits=FAKE, probs=FAKE, unif=FAKE, temp=1.0, B=2, N=8, V=100, ws=FAKE * 256, wsb=1 << 30):
+        return lib.tree_accept(logits, FAKE, probs, FAKE, unif, ctypes.c_float(temp), FAKE, FAKE, FAKE,
+                               B, N, V, ws, wsb, None)
+
+    assert call(N=65) == -2
+    assert call(B=0) == -2
+    assert call(V=0) == -2
+    assert call(logits=None) == -1
+    assert call(temp=-1.0) == -5
+    assert call(temp=float("nan")) == -5
+    assert call(probs=None) == -5
+    assert call(unif=None) == -5
+    assert call(logits=FAKE + 8) == -6
+    assert call(ws=FAKE + 64) == -4
+    assert call(wsb=16) == -4
+    assert lib.treespec_accept_workspace_bytes(2, 65, 100) == 0
+
+
+def test_valid_call_without_device_reports_no_device():
+    """Every host check passes; with no GPU present the call stops at the device check."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    prob = shape()
+    lib = ts.raw_library()
+    rc = lib.tree_attn_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(prob.c_shape()),
+                              FAKE * 256, 1 << 30, None)
+    assert rc == -7

@@ -1,0 +1,149 @@
+"""GPU parity of tree_attn_verify against the float64 oracle (through the C-ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from gen import inputs as gi
+from gen import trees
+
+from gpu_util import (assert_attention_close, attn_device_inputs, dev_tensor, oracle_attention)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ts():
+    import __graft_entry__
+    __graft_entry__.build()
+    import eagle_speculative_tree_gb300 as mod
+    return mod
+
+
+def run(ts, x, device, **kw):
+    d = attn_device_inputs(x, device)
+    out = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"],
+                              d["tree_parents"], **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+SMALL = [
+    ("c1_tiny_f32_greedy", None),
+    ("c2_llama3_8b_bf16_greedy", None),
+    ("c3_llama2_7b_bf16_stoch", 2),
+    ("c4_llama3_70b_bf16_greedy", 1),
+    ("c5_ragged_b64_bf16_stoch", 3),
+]
+
+
+@pytest.mark.parametrize("name,batch", SMALL)
+def test_configs_match_oracle(ts, cuda_device, name, batch):
+    w = gen.get(name)
+    if batch is not None:
+        w = w.with_batch(batch)
+    x = gi.make_inputs(w, with_accept=False)
+    out = run(ts, x, cuda_device)
+    assert_attention_close(out, oracle_attention(x), w.dtype)
+
+
+@pytest.mark.parametrize("kernel", [1])
+@pytest.mark.parametrize("splits", [1, 3, 40])
+def test_split_counts(ts, cuda_device, kernel, splits):
+    w = gen.get("c2_llama3_8b_bf16_greedy")
+    x = gi.make_inputs(w, with_accept=False)
+    out = run(ts, x, cuda_device, kernel=kernel, num_splits=splits)
+    assert_attention_close(out, oracle_attention(x), w.dtype)
+
+
+def _custom(name, parents, prefix, batch=None):
+    w = gen.get(name)
+    parents = np.asarray(parents, dtype=np.int32)
+    w = w.with_batch(batch or parents.shape[0])
+    from dataclasses import replace
+    w = replace(w, num_nodes=parents.shape[1])
+    return w, gi.make_inputs(w, parents=parents, prefix_lens=np.asarray(prefix, dtype=np.int32),
+                             with_accept=False)
+
+
+@pytest.mark.parametrize("dtype_cfg", ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy"])
+@pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
+                                  "random64"])
+def test_edge_cases(ts, cuda_device, dtype_cfg, case):
+    rng = np.random.default_rng(hash(case) % 2**32)
+    if case == "single_node":
+        parents, prefix = [[-1], [-1]], [37, 0]
+    elif case == "prefix0":
+        parents, prefix = [trees.random_recursive(rng, 9)], [0]
+    elif case == "ragged_tail":
+        parents, prefix = [trees.random_recursive(rng, 11), trees.chain(11)], [17, 301]
+    elif case == "chain64":
+        parents, prefix = [trees.chain(64)], [129]
+    elif case == "star64":
+        parents, prefix = [trees.star(64)], [40]
+    else:
+        parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
+    w, x = _custom(dtype_cfg, parents, prefix)
+    out = run(ts, x, cuda_device)
+    assert_attention_close(out, oracle_attention(x), w.dtype)
+
+
+def test_bad_parents_and_lengths_are_flagged(ts, cuda_device):
+    w = gen.get("c2_llama3_8b_bf16_greedy").with_batch(2)
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    bad_parents = d["tree_parents"].clone()
+    bad_parents[0, 3] = 5                          # not an earlier node
+    ws = torch.empty(ts.attn_workspace_bytes(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])),
+                     dtype=torch.uint8, device=cuda_device)
+    ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"], bad_parents,
+                        workspace=ws)
+    assert ts.read_status(ws) & 1
+    bad_len = d["prefix_lens"].clone()
+    bad_len[1] = 10 ** 6
+    out = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], bad_len,
+                              d["tree_parents"], workspace=ws)
+    assert ts.read_status(ws) & 4
+    assert torch.all(out[1] == 0)
+    out = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"],
+                              d["tree_parents"], workspace=ws)
+    assert ts.read_status(ws) == 0
+    assert_attention_close(out, oracle_attention(x), w.dtype)
+
+
+def test_bad_page_id_is_flagged_not_read(ts, cuda_device):
+    w = gen.get("c1_tiny_f32_greedy")
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    d["page_table"][0, 1] = 1 << 30
+    ws = torch.empty(ts.attn_workspace_bytes(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])),
+                     dtype=torch.uint8, device=cuda_device)
+    ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"],
+                        d["tree_parents"], workspace=ws)
+    assert ts.read_status(ws) & 2
+
+
+def test_full_size_bench_workload_sampled(ts, cuda_device):
+    """The bench's workload at full size; the oracle checks sampled (sequence, kv head) pairs."""
+    w = gen.get("c4_llama3_70b_bf16_greedy")
+    x = gi.make_inputs(w, with_accept=False)
+    out = run(ts, x, cuda_device)
+    rng = np.random.default_rng(0)
+    pairs = [(int(b), int(h)) for b, h in zip(rng.integers(0, w.batch, 3), rng.integers(0, w.num_kv_heads, 3))]
+    ref = oracle_attention(x, pairs)
+    mask = ~np.isnan(ref)
+    assert mask.sum() > 0
+    assert_attention_close(out, ref, w.dtype, mask=mask)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_full_size_ragged_sampled(ts, cuda_device):
+    w = gen.get("c5_ragged_b64_bf16_stoch")
+    x = gi.make_inputs(w, with_accept=False)
+    out = run(ts, x, cuda_device)
+    order = np.argsort(x.prefix_lens)
+    pairs = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 3)]
+    ref = oracle_attention(x, pairs)
+    mask = ~np.isnan(ref)
+    assert_attention_close(out, ref, w.dtype, mask=mask)
+    assert torch.isfinite(out.float()).all()
