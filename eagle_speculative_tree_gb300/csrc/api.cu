@@ -64,7 +64,10 @@ int check_attn_shape(const treespec_attn_shape* s) {
     if (R > 4096 || (long long)s->num_kv_heads * ((R + 63) / 64) > 65535) return TREESPEC_ERR_SHAPE;
     if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC) return TREESPEC_ERR_SHAPE;
     if (s->num_splits < 0) return TREESPEC_ERR_SHAPE;
-    if (s->kernel == TREESPEC_KERNEL_TC) return TREESPEC_ERR_DTYPE;   // not built in this library yet
+    if (s->kernel == TREESPEC_KERNEL_TC) {
+        if (!attn_tc_supported(s->dtype, s->head_dim)) return TREESPEC_ERR_DTYPE;
+        if ((long long)s->num_pool_pages * s->page_size >= (1ll << 31)) return TREESPEC_ERR_SHAPE;
+    }
     return TREESPEC_OK;
 }
 
@@ -72,8 +75,15 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     AttnPlan p{};
     const int G = s.num_q_heads / s.num_kv_heads;
     const int R = s.num_nodes * G;
-    p.kernel = TREESPEC_KERNEL_SIMT;
-    p.rows_per_block = R < 64 ? R : 64;
+    const bool tc_ok = attn_tc_supported(s.dtype, s.head_dim) &&
+                       (long long)s.num_pool_pages * s.page_size < (1ll << 31);
+    if (s.kernel == TREESPEC_KERNEL_TC || (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok && R >= 64)) {
+        p.kernel = TREESPEC_KERNEL_TC;
+        p.rows_per_block = 128;
+    } else {
+        p.kernel = TREESPEC_KERNEL_SIMT;
+        p.rows_per_block = R < 64 ? R : 64;
+    }
     p.row_blocks = (R + p.rows_per_block - 1) / p.rows_per_block;
     const long long max_tokens = (long long)s.max_pages_per_seq * s.page_size;
     const int tile = 128;                       // split sizes are multiples of every tile size
@@ -220,7 +230,8 @@ extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* 
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     if (launch_tree_prologue(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches++;
-    if (launch_attn_simt(p, s.dtype, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    const cudaError_t e = plan.kernel == TREESPEC_KERNEL_TC ? launch_attn_tc(p, st) : launch_attn_simt(p, s.dtype, st);
+    if (e != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches++;
     if (plan.merge) {
         if (launch_attn_merge(p, s.dtype, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;

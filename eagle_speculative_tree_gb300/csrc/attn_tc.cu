@@ -1,0 +1,451 @@
+// Split-KV paged tree attention on the 5th-generation tensor cores (bf16, head_dim 128).
+//
+// Same partial state as the CUDA-core kernel (m, l, acc per query row of one split),
+// computed with tcgen05:
+//   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
+//     are zero) x one split of the sequence's logical tokens;
+//   * warp 0 streams the split's K and V pages with TMA (one 16-token page x 64
+//     head-dim columns per copy, 128-byte swizzle) into a two-stage ring; the partly
+//     filled last page of a sequence and pages past the split are written by the warp
+//     itself, zero-filled, so nothing outside the sequence reaches the MMA;
+//   * warp 1 allocates TMEM (S double buffer + O) and issues S = Q K^T and O += P V as
+//     128x128x16 tcgen05.mma instructions from shared-memory descriptors;
+//   * warps 2-5 (one TMEM lane quarter each, one query row per thread) read S from
+//     TMEM, apply the tree mask -- prefix tokens always, tree token S+j only when bit
+//     j of the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2
+//     mask M and section 5 bitmask) -- run the online softmax in base 2, write P as
+//     bf16 to shared memory, and rescale O in TMEM only when a row's running max grows
+//     by more than 2^8.
+// Every mbarrier wait is bounded; on expiry the CTA records TREESPEC_STATUS_TIMEOUT,
+// drains its own tensor-core work, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace treespec {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kM = 128;              // query rows per CTA = TMEM lanes
+constexpr int kD = 128;              // head dim
+constexpr int kBN = 128;             // tokens per tile
+constexpr int kNS = 2;               // K/V ring stages
+constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
+constexpr int kTile = 2 * kPanel;    // [128][128] bf16
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+// shared-memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kNS * kTile;
+constexpr int kOffP = kOffV + kNS * kTile;
+constexpr int kOffBar = kOffP + kTile;
+constexpr int kNumBars = 2 * kNS + 2 + 2 + 4;   // kv_full, kv_empty, s_full, s_empty, p_full, o_done, q_full, drain
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kOffAnc = (kOffMisc + 16 + 7) / 8 * 8;
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8 + 1024;   // + alignment slack
+
+struct Bars {
+    uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], s_empty[2], p_full, o_done, q_full, drain;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+    volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
+    uint64_t* anc_s = reinterpret_cast<uint64_t*>(sm + kOffAnc);
+
+    const int split = blockIdx.x;
+    const int h = blockIdx.y / p.row_blocks, rb = blockIdx.y % p.row_blocks;
+    const int b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = rb * kM;
+    const int S = p.lens[b];
+
+    if (S < 0) {                                   // invalid sequence: zeros (or the merge writes them)
+        if (!p.merge && split == 0) {
+            for (int e = tid; e < kM * (kD / 8); e += kThreads) {
+                const int row = r0 + e / (kD / 8), c = e % (kD / 8);
+                if (row >= p.R) continue;
+                const int i = row / p.G, hq = h * p.G + row % p.G;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                      ((size_t(b) * p.N + i) * p.Hq + hq) * kD) + c;
+                *dst = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+    const int L = S + p.N;
+    const int t0 = split * p.split_tokens;
+    const int t1 = min(L, t0 + p.split_tokens);
+    if (t0 >= t1) return;
+    const int ntiles = (t1 - t0 + kBN - 1) / kBN;
+
+    if (tid == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(&bars->kv_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->s_empty[s], 128);
+        }
+        mbar_init(&bars->p_full, 128);
+        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->q_full, 128);
+        mbar_init(&bars->drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int e = tid; e < p.N; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N + e];
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        const int* ptab = p.page_table + size_t(b) * p.max_pages;
+        if (lane == 0) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
+        for (int j = 0; j < ntiles; ++j) {
+            const int stage = j % kNS;
+            if (j >= kNS && !mbar_wait_bounded(&bars->kv_empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+            }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            const int base = t0 + j * kBN;
+            // classify the tile's 8 pages: 1 = TMA, 2 = written here (partial / bad / absent)
+            int page = -1, kind = 2;
+            if (lane < 8) {
+                const int pos0 = base + lane * 16;
+                if (pos0 < t1) {
+                    page = ptab[pos0 >> 4];
+                    const bool ok = page >= 0 && page < p.num_pool_pages;
+                    if (!ok) atomicOr(p.status, TREESPEC_STATUS_BAD_PAGE);
+                    kind = (ok && pos0 + 16 <= L) ? 1 : 2;
+                    if (!ok) page = -1;
+                }
+            }
+            unsigned char* Ks = sm + kOffK + stage * kTile;
+            unsigned char* Vs = sm + kOffV + stage * kTile;
+            const unsigned manual = __ballot_sync(0xffffffffu, lane < 8 && kind == 2);
+            for (int pg = 0; pg < 8; ++pg) {
+                if (!((manual >> pg) & 1u)) continue;
+                const int pgid = __shfl_sync(0xffffffffu, page, pg);
+                const int pos0 = base + pg * 16;
+                for (int c = lane; c < 16 * 16; c += 32) {      // 16 token rows x 16 chunks of 16 bytes
+                    const int rr = c >> 4, ch = c & 15;
+                    const int pos = pos0 + rr;
+                    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+                    if (pgid >= 0 && pos < t1) {
+                        const size_t off = ((size_t(pgid) * p.ps + (pos & 15)) * p.Hkv + h) * kD + ch * 8;
+                        kv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k) + off));
+                        vv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v) + off));
+                    }
+                    const uint32_t o = (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7);
+                    *reinterpret_cast<uint4*>(Ks + o) = kv;
+                    *reinterpret_cast<uint4*>(Vs + o) = vv;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const unsigned viatma = __ballot_sync(0xffffffffu, lane < 8 && kind == 1);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->kv_full[stage], uint32_t(__popc(viatma)) * 4u * 2048u);
+            }
+            for (int pg = 0; pg < 8; ++pg) {
+                const int pgid = __shfl_sync(0xffffffffu, page, pg);
+                if (lane == 0 && ((viatma >> pg) & 1u)) {
+                    const int z = pgid * 16;
+                    tma_load_3d(Ks + pg * 2048, &tmk, 0, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(Ks + kPanel + pg * 2048, &tmk, 64, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(Vs + pg * 2048, &tmv, 0, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(Vs + kPanel + pg * 2048, &tmv, 64, h, z, &bars->kv_full[stage]);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
+            constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
+            const uint32_t qaddr = sbase + kOffQ, paddr = sbase + kOffP;
+            bool ok = mbar_wait_bounded(&bars->q_full, 0, kWaitNs);
+            auto issue_s = [&](int j) -> bool {
+                const int stage = j % kNS;
+                if (!mbar_wait_bounded(&bars->kv_full[stage], (j / kNS) & 1, kWaitNs)) return false;
+                if (j >= 2 && !mbar_wait_bounded(&bars->s_empty[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) return false;
+                tc_fence_after();
+                const uint32_t kaddr = sbase + kOffK + stage * kTile;
+                const uint32_t d = tbase + uint32_t(j & 1) * 128u;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * kPanel + (kk & 3) * 32;
+                    mma_bf16_ss(d, smem_desc(qaddr + koff, 16, 1024), smem_desc(kaddr + koff, 16, 1024), kIdS,
+                                kk > 0);
+                }
+                mma_commit(&bars->s_full[j & 1]);
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                if (!mbar_wait_bounded(&bars->p_full, j & 1, kWaitNs)) return false;
+                tc_fence_after();
+                const int stage = j % kNS;
+                const uint32_t vaddr = sbase + kOffV + stage * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint32_t poff = (kk >> 2) * kPanel + (kk & 3) * 32;
+                    mma_bf16_ss(tbase + 256u, smem_desc(paddr + poff, 16, 1024),
+                                smem_desc(vaddr + kk * 2048, kPanel, 1024), kIdO, (j > 0 || kk > 0));
+                }
+                mma_commit(&bars->kv_empty[stage]);
+                mma_commit(&bars->o_done);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                if (*abort_flag) { ok = false; break; }
+                if (j + 1 < ntiles) ok = issue_s(j + 1);
+                if (ok) ok = issue_pv(j);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+            }
+            mma_commit(&bars->drain);                        // everything issued above has finished
+            mbar_wait_bounded(&bars->drain, 0, kWaitNs);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;                   // query row in the block = TMEM lane
+        const int r = r0 + t;
+        const bool row_ok = r < p.R;
+        const int i = row_ok ? r / p.G : 0;
+        const int hq = h * p.G + (row_ok ? r % p.G : 0);
+        const uint64_t anc = row_ok ? anc_s[i] : 0ull;
+        const bool warp_rows = __any_sync(0xffffffffu, row_ok);
+        const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
+        {
+            const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                               ((size_t(b) * p.N + i) * p.Hq + hq) * kD);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = row_ok ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + kOffQ + (c >> 3) * kPanel + sw128_offset(t, c & 7)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_full);
+
+        const float sc = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool alive = true;
+        for (int j = 0; j < ntiles && alive; ++j) {
+            const int base = t0 + j * kBN;
+            if (!mbar_wait_bounded(&bars->s_full[j & 1], (j >> 1) & 1, kWaitNs)) { alive = false; break; }
+            tc_fence_after();
+            // columns of this tile a row may see: prefix columns below pref_end, tree
+            // columns [tree_lo, tree_hi) through the node's ancestor word
+            const int pref_end = min(S, t1) - base;
+            const int tree_lo = S - base, tree_hi = t1 - base;
+            const uint32_t scol = tl + uint32_t(j & 1) * 128u;
+            auto masked = [&](int col, uint32_t raw) -> float {
+                const bool ok = row_ok && (col < pref_end ||
+                                           (col >= tree_lo && col < tree_hi && ((anc >> (col - tree_lo)) & 1ull)));
+                return ok ? __uint_as_float(raw) * sc : -INFINITY;
+            };
+            // pass 1: tile max
+            float mt = -INFINITY;
+            if (warp_rows) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(scol + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mt = fmaxf(mt, masked(c * 32 + e, v[e]));
+                }
+            }
+            bool resc = false;
+            float alpha = 1.f;
+            if (mt > m_used + 8.f) {
+                alpha = ex2(m_used - mt);
+                resc = m_used != -INFINITY;
+                l *= alpha;
+                m_used = mt;
+            }
+            const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+            // pass 2: probabilities, rounded to bf16 and packed in pairs
+            uint32_t pk[kBN / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                if (warp_rows) {
+                    tmem_ld32(scol + c * 32, v);
+                    tmem_wait_ld();
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const uint32_t w = pack_bf16x2(ex2(masked(c * 32 + 2 * e, v[2 * e]) - msub),
+                                                   ex2(masked(c * 32 + 2 * e + 1, v[2 * e + 1]) - msub));
+                    pk[c * 16 + e] = w;
+                    lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->s_empty[j & 1]);
+            l += lsum;
+            // P buffer and O are free once P_{j-1} V_{j-1} has completed
+            if (j > 0 && !mbar_wait_bounded(&bars->o_done, (j - 1) & 1, kWaitNs)) { alive = false; break; }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, resc)) {
+                const float f = resc ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tl + 256u + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tmem_st32(tl + 256u + c * 32, o);
+                }
+                tmem_wait_st();
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<uint4*>(sm + kOffP + (c >> 3) * kPanel + sw128_offset(t, c & 7)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full);
+        }
+        if (!alive) {
+            *abort_flag = 1;
+            atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+        } else if (mbar_wait_bounded(&bars->o_done, (ntiles - 1) & 1, kWaitNs)) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                if (warp_rows) {
+                    tmem_ld32(tl + 256u + c * 32, o);
+                    tmem_wait_ld();
+                }
+                if (!row_ok) continue;
+                if (!p.merge) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                          ((size_t(b) * p.N + i) * p.Hq + hq) * kD + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k2 = 0; k2 < 4; ++k2) {
+                            const int idx = e * 8 + k2 * 2;
+                            w4[k2] = pack_bf16x2(__uint_as_float(o[idx]) * inv, __uint_as_float(o[idx + 1]) * inv);
+                        }
+                        dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                } else {
+                    const size_t pr = (size_t(b * p.Hkv + h) * p.num_splits + split) * p.R + r;
+                    float4* dst = reinterpret_cast<float4*>(p.part_acc + pr * kD + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                             __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    if (c == 0) {
+                        p.part_ml[pr * 2] = m_used;
+                        p.part_ml[pr * 2 + 1] = l;
+                    }
+                }
+            }
+        } else {
+            *abort_flag = 1;
+            atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D view of a page pool [P][16][Hkv][128] bf16 as (head dim, kv head, pool token),
+// copied in boxes of 64 head-dim columns x 1 head x 16 tokens (one page) with
+// 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_tokens) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(Hkv), cuuint64_t(pool_tokens)};
+    cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(Hkv) * kD * 2};
+    cuuint32_t box[3] = {64, 1, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_tc_supported(int dtype, int D) { return dtype == TREESPEC_DTYPE_BF16 && D == kD; }
+
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
+    CUtensorMap mk, mv;
+    const long long pool_tokens = (long long)p.num_pool_pages * p.ps;
+    if (!make_pool_map(&mk, p.k, p.Hkv, pool_tokens) || !make_pool_map(&mv, p.v, p.Hkv, pool_tokens))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.num_splits, p.Hkv * p.row_blocks, p.B);
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, mk, mv);
+    return cudaGetLastError();
+}
+
+}  // namespace treespec

@@ -101,6 +101,8 @@ struct AcceptParams {
 // Kernel launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_tree_prologue(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
+bool attn_tc_supported(int dtype, int D);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s);
 size_t attn_simt_smem_bytes(int dtype, int D, int R_block);

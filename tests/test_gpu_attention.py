@@ -37,17 +37,30 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 @pytest.mark.parametrize("name,batch", SMALL)
-def test_configs_match_oracle(ts, cuda_device, name, batch):
+def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
     w = gen.get(name)
     if batch is not None:
         w = w.with_batch(batch)
+    if kernel == 2 and w.dtype != "bf16":
+        pytest.skip("the tensor-core kernel takes bf16")
     x = gi.make_inputs(w, with_accept=False)
-    out = run(ts, x, cuda_device)
+    out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
 
 
-@pytest.mark.parametrize("kernel", [1])
+def test_auto_plan_picks_tensor_cores_from_64_rows(ts, cuda_device):
+    for name, want in [("c2_llama3_8b_bf16_greedy", 1), ("c3_llama2_7b_bf16_stoch", 1),
+                       ("c4_llama3_70b_bf16_greedy", 2), ("c5_ragged_b64_bf16_stoch", 2),
+                       ("c1_tiny_f32_greedy", 1)]:
+        w = gen.get(name)
+        prob = ts.AttnProblem(w.batch, w.num_nodes, w.num_q_heads, w.num_kv_heads, w.head_dim, 16, 64, 100,
+                              ts.DTYPE_BF16 if w.dtype == "bf16" else ts.DTYPE_F32)
+        assert ts.attn_plan(prob).kernel == want, name
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("splits", [1, 3, 40])
 def test_split_counts(ts, cuda_device, kernel, splits):
     w = gen.get("c2_llama3_8b_bf16_greedy")
@@ -66,10 +79,11 @@ def _custom(name, parents, prefix, batch=None):
                              with_accept=False)
 
 
-@pytest.mark.parametrize("dtype_cfg", ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy"])
+@pytest.mark.parametrize("dtype_cfg,kernel", [("c1_tiny_f32_greedy", 1), ("c2_llama3_8b_bf16_greedy", 1),
+                                              ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2)])
 @pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
                                   "random64"])
-def test_edge_cases(ts, cuda_device, dtype_cfg, case):
+def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
     rng = np.random.default_rng(hash(case) % 2**32)
     if case == "single_node":
         parents, prefix = [[-1], [-1]], [37, 0]
@@ -84,7 +98,7 @@ def test_edge_cases(ts, cuda_device, dtype_cfg, case):
     else:
         parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
     w, x = _custom(dtype_cfg, parents, prefix)
-    out = run(ts, x, cuda_device)
+    out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
 
 
@@ -127,6 +141,8 @@ def test_full_size_bench_workload_sampled(ts, cuda_device):
     """The bench's workload at full size; the oracle checks sampled (sequence, kv head) pairs."""
     w = gen.get("c4_llama3_70b_bf16_greedy")
     x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    assert ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])).kernel == ts.KERNEL_TC
     out = run(ts, x, cuda_device)
     rng = np.random.default_rng(0)
     pairs = [(int(b), int(h)) for b, h in zip(rng.integers(0, w.batch, 3), rng.integers(0, w.num_kv_heads, 3))]
