@@ -26,6 +26,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC = 0, 1, 2
+ACCEPT_AUTO, ACCEPT_ALL_ROWS, ACCEPT_PATH_ONLY = 0, 1, 2
 STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT"}
 
 
@@ -52,6 +53,9 @@ _lib.treespec_accept_workspace_bytes.restype = ctypes.c_size_t
 _lib.tree_accept.argtypes = [_vp] * 5 + [ctypes.c_float] + [_vp] * 3 + [ctypes.c_int32] * 3 + \
     [_vp, ctypes.c_size_t, _vp]
 _lib.tree_accept.restype = ctypes.c_int
+_lib.tree_accept_with_mode.argtypes = [_vp] * 5 + [ctypes.c_float] + [_vp] * 3 + [ctypes.c_int32] * 4 + \
+    [_vp, ctypes.c_size_t, _vp]
+_lib.tree_accept_with_mode.restype = ctypes.c_int
 _lib.treespec_read_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
 _lib.treespec_read_status.restype = ctypes.c_int
 _lib.treespec_error_string.argtypes = [ctypes.c_int]
@@ -187,9 +191,11 @@ def accept_workspace_bytes(batch: int, num_nodes: int, vocab: int) -> int:
 
 
 def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms, temperature: float, *,
-                accept_path=None, accept_len=None, bonus_token=None,
+                accept_path=None, accept_len=None, bonus_token=None, mode: int = ACCEPT_AUTO,
                 workspace: Optional[torch.Tensor] = None, stream=None):
-    """Accept walk; see include/treespec.h.  Returns (accept_path, accept_len, bonus_token)."""
+    """Accept walk; see include/treespec.h.  Returns (accept_path, accept_len, bonus_token).
+
+    mode: ACCEPT_AUTO, ACCEPT_ALL_ROWS or ACCEPT_PATH_ONLY (tree_accept_with_mode)."""
     dev = target_logits.device
     B, N, V = target_logits.shape
     _need(target_logits, "target_logits", torch.float32, dev)
@@ -207,10 +213,10 @@ def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms
     need = accept_workspace_bytes(B, N, V)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    _check(_lib.tree_accept(
+    _check(_lib.tree_accept_with_mode(
         _ptr(target_logits), _ptr(draft_tokens), _ptr(draft_probs) if temperature > 0 else None,
         _ptr(tree_parents), _ptr(uniforms) if temperature > 0 else None, float(temperature),
-        _ptr(accept_path), _ptr(accept_len), _ptr(bonus_token), B, N, V,
+        _ptr(accept_path), _ptr(accept_len), _ptr(bonus_token), B, N, V, int(mode),
         _ptr(workspace), workspace.numel(), _stream_handle(stream, dev)))
     return accept_path, accept_len, bonus_token
 

@@ -98,7 +98,7 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     }
     long long chunk = (max_tokens + splits - 1) / splits;
     chunk = (chunk + tile - 1) / tile * tile;
-    if (s.num_splits == 0 && chunk > 4096) chunk = 4096;     // bounded CTA length (ragged batches)
+    if (s.num_splits == 0 && chunk > 16384) chunk = 16384;   // bounded CTA length (ragged batches)
     if (chunk < tile) chunk = tile;
     p.split_tokens = int(chunk);
     p.num_splits = int((max_tokens + chunk - 1) / chunk);
@@ -245,15 +245,16 @@ extern "C" size_t treespec_accept_workspace_bytes(int32_t batch, int32_t num_nod
     return accept_layout(batch, num_nodes).total;
 }
 
-extern "C" int tree_accept(const float* target_logits, const int32_t* draft_tokens,
-                           const float* draft_probs, const int32_t* tree_parents,
-                           const float* uniforms, float temperature, int32_t* accept_path,
-                           int32_t* accept_len, int32_t* bonus_token, int32_t batch,
-                           int32_t num_nodes, int32_t vocab, void* workspace,
-                           size_t workspace_bytes, treespec_stream_t stream) {
+extern "C" int tree_accept_with_mode(const float* target_logits, const int32_t* draft_tokens,
+                                     const float* draft_probs, const int32_t* tree_parents,
+                                     const float* uniforms, float temperature, int32_t* accept_path,
+                                     int32_t* accept_len, int32_t* bonus_token, int32_t batch,
+                                     int32_t num_nodes, int32_t vocab, int32_t mode, void* workspace,
+                                     size_t workspace_bytes, treespec_stream_t stream) {
     if (batch < 1 || num_nodes < 1 || num_nodes > kMaxNodes || vocab < 1 || vocab > (1 << 30))
         return TREESPEC_ERR_SHAPE;
     if ((long long)batch * num_nodes > 0x7fffffffll) return TREESPEC_ERR_SHAPE;
+    if (mode < TREESPEC_ACCEPT_AUTO || mode > TREESPEC_ACCEPT_PATH_ONLY) return TREESPEC_ERR_SHAPE;
     if (!target_logits || !draft_tokens || !tree_parents || !accept_path || !accept_len || !bonus_token)
         return TREESPEC_ERR_NULL_POINTER;
     if (!(temperature >= 0.f) || std::isinf(temperature)) return TREESPEC_ERR_SAMPLING;
@@ -265,6 +266,9 @@ extern "C" int tree_accept(const float* target_logits, const int32_t* draft_toke
     if (workspace_bytes < lay.total) return TREESPEC_ERR_WORKSPACE;
     const int rc = check_device();
     if (rc != TREESPEC_OK) return rc;
+    if (mode == TREESPEC_ACCEPT_AUTO)
+        mode = (long long)batch * num_nodes * vocab > (1ll << 24) ? TREESPEC_ACCEPT_PATH_ONLY
+                                                                 : TREESPEC_ACCEPT_ALL_ROWS;
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     AcceptParams p{};
@@ -287,9 +291,21 @@ extern "C" int tree_accept(const float* target_logits, const int32_t* draft_toke
     p.inv_t = stoch ? 1.f / temperature : 0.f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
-    if (launch_accept(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
-    g_launches += 2;
+    int kernels = 0;
+    if (launch_accept(p, mode, st, &kernels) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches += kernels;
     return TREESPEC_OK;
+}
+
+extern "C" int tree_accept(const float* target_logits, const int32_t* draft_tokens,
+                           const float* draft_probs, const int32_t* tree_parents,
+                           const float* uniforms, float temperature, int32_t* accept_path,
+                           int32_t* accept_len, int32_t* bonus_token, int32_t batch,
+                           int32_t num_nodes, int32_t vocab, void* workspace,
+                           size_t workspace_bytes, treespec_stream_t stream) {
+    return tree_accept_with_mode(target_logits, draft_tokens, draft_probs, tree_parents, uniforms, temperature,
+                                 accept_path, accept_len, bonus_token, batch, num_nodes, vocab,
+                                 TREESPEC_ACCEPT_AUTO, workspace, workspace_bytes, stream);
 }
 
 extern "C" int treespec_read_status(const void* workspace, uint32_t* status, treespec_stream_t stream) {

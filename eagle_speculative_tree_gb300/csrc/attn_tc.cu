@@ -132,8 +132,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
         }
+        // page ids of tile j (lane k < 8 holds page k of the tile), fetched one tile ahead
+        auto fetch_pages = [&](int j) -> int {
+            const int pos0 = t0 + j * kBN + lane * 16;
+            return (lane < 8 && j < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
+        };
+        int page_next = fetch_pages(0);
         for (int j = 0; j < ntiles; ++j) {
             const int stage = j % kNS;
+            int page = page_next;
+            page_next = fetch_pages(j + 1);
             if (j >= kNS && !mbar_wait_bounded(&bars->kv_empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
@@ -141,11 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             const int base = t0 + j * kBN;
             // classify the tile's 8 pages: 1 = TMA, 2 = written here (partial / bad / absent)
-            int page = -1, kind = 2;
+            int kind = 2;
             if (lane < 8) {
                 const int pos0 = base + lane * 16;
                 if (pos0 < t1) {
-                    page = ptab[pos0 >> 4];
                     const bool ok = page >= 0 && page < p.num_pool_pages;
                     if (!ok) atomicOr(p.status, TREESPEC_STATUS_BAD_PAGE);
                     kind = (ok && pos0 + 16 <= L) ? 1 : 2;
@@ -273,28 +280,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int base = t0 + j * kBN;
             if (!mbar_wait_bounded(&bars->s_full[j & 1], (j >> 1) & 1, kWaitNs)) { alive = false; break; }
             tc_fence_after();
-            // columns of this tile a row may see: prefix columns below pref_end, tree
-            // columns [tree_lo, tree_hi) through the node's ancestor word
+            // which of the tile's 128 columns this row may see, as four 32-bit words:
+            // prefix columns below pref_end, tree columns [tree_lo, tree_hi) through the
+            // node's ancestor word
             const int pref_end = min(S, t1) - base;
             const int tree_lo = S - base, tree_hi = t1 - base;
-            const uint32_t scol = tl + uint32_t(j & 1) * 128u;
-            auto masked = [&](int col, uint32_t raw) -> float {
-                const bool ok = row_ok && (col < pref_end ||
-                                           (col >= tree_lo && col < tree_hi && ((anc >> (col - tree_lo)) & 1ull)));
-                return ok ? __uint_as_float(raw) * sc : -INFINITY;
-            };
-            // pass 1: tile max
-            float mt = -INFINITY;
-            if (warp_rows) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(scol + c * 32, v);
-                    tmem_wait_ld();
+            uint32_t mw[4];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mt = fmaxf(mt, masked(c * 32 + e, v[e]));
-                }
+            for (int w = 0; w < 4; ++w) {
+                const int lo = 32 * w;
+                const int np = min(max(pref_end - lo, 0), 32);
+                uint32_t bits = np == 32 ? 0xffffffffu : ((1u << np) - 1u);
+                const int nh = min(max(tree_hi - lo, 0), 32);
+                const uint32_t hi_mask = nh == 32 ? 0xffffffffu : ((1u << nh) - 1u);
+                uint32_t tb = 0;
+                const int sh = lo - tree_lo;               // anc bit index of column lo
+                if (sh >= 0) tb = sh < 64 ? uint32_t(anc >> sh) : 0u;
+                else tb = -sh < 32 ? uint32_t(anc << (-sh)) : 0u;
+                bits |= tb & hi_mask;
+                mw[w] = row_ok ? bits : 0u;
             }
+            const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu);
+            // raw scores of the whole row in one TMEM round trip, masked in place
+            uint32_t v[kBN];
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + uint32_t(j & 1) * 128u + c * 32, v + c * 32);
+                tmem_wait_ld();
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->s_empty[j & 1]);            // S buffer reusable from here
+            constexpr uint32_t kNegInf = 0xff800000u;
+            if (!full) {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+            const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float mt = mraw * sc;                    // scale > 0 commutes with max
             bool resc = false;
             float alpha = 1.f;
             if (mt > m_used + 8.f) {
@@ -304,26 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = mt;
             }
             const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-            // pass 2: probabilities, rounded to bf16 and packed in pairs
-            uint32_t pk[kBN / 2];
-            float lsum = 0.f;
+            // probabilities 2^(s*scale - m), rounded to bf16 and packed in pairs
+            // (packed in place: pair c lands in v[c], after v[2c] and v[2c+1] were read)
+            uint32_t* pk = v;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                if (warp_rows) {
-                    tmem_ld32(scol + c * 32, v);
-                    tmem_wait_ld();
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const uint32_t w = pack_bf16x2(ex2(masked(c * 32 + 2 * e, v[2 * e]) - msub),
-                                                   ex2(masked(c * 32 + 2 * e + 1, v[2 * e + 1]) - msub));
-                    pk[c * 16 + e] = w;
-                    lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-                }
+            for (int c = 0; c < kBN / 2; ++c) {
+                const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, -msub));
+                const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, -msub));
+                pk[c] = pack_bf16x2(p0, p1);
+                ls[c & 3] += p0 + p1;
             }
-            tc_fence_before();
-            mbar_arrive(&bars->s_empty[j & 1]);
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l += lsum;
             // P buffer and O are free once P_{j-1} V_{j-1} has completed
             if (j > 0 && !mbar_wait_bounded(&bars->o_done, (j - 1) & 1, kWaitNs)) { alive = false; break; }

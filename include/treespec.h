@@ -55,6 +55,12 @@ enum treespec_kernel {
     TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128) */
 };
 
+enum treespec_accept_mode {
+    TREESPEC_ACCEPT_AUTO = 0,       /* path-only when B*N*V is large, all rows otherwise */
+    TREESPEC_ACCEPT_ALL_ROWS = 1,   /* reduce every (sequence, node) row, then walk */
+    TREESPEC_ACCEPT_PATH_ONLY = 2,  /* walk first; reduce only the rows the walk visits */
+};
+
 enum treespec_error {
     TREESPEC_OK = 0,
     TREESPEC_ERR_NULL_POINTER = -1,   /* a required pointer is NULL */
@@ -178,6 +184,18 @@ int tree_accept(const float *target_logits, const int32_t *draft_tokens,
                 int32_t *accept_path, int32_t *accept_len, int32_t *bonus_token,
                 int32_t batch, int32_t num_nodes, int32_t vocab,
                 void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
+/*
+ * tree_accept_with_mode -- tree_accept with an explicit schedule (enum treespec_accept_mode).
+ * Both schedules return identical results; they differ in which rows they read: all
+ * B*N rows up front, or only the rows on each sequence's walk.
+ */
+int tree_accept_with_mode(const float *target_logits, const int32_t *draft_tokens,
+                          const float *draft_probs, const int32_t *tree_parents,
+                          const float *uniforms, float temperature,
+                          int32_t *accept_path, int32_t *accept_len, int32_t *bonus_token,
+                          int32_t batch, int32_t num_nodes, int32_t vocab, int32_t mode,
+                          void *workspace, size_t workspace_bytes, treespec_stream_t stream);
 
 /* ------------------------------------------------------------------------- helpers */
 

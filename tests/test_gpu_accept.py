@@ -21,21 +21,22 @@ def ts():
     return mod
 
 
-def run(ts, x, device):
+def run(ts, x, device, mode=0):
     d = accept_device_inputs(x, device)
     res = ts.tree_accept(d["target_logits"], d["draft_tokens"], d["draft_probs"], d["tree_parents"],
-                         d["uniforms"], x.temperature)
+                         d["uniforms"], x.temperature, mode=mode)
     torch.cuda.synchronize()
     return res
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("name", ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy",
                                   "c3_llama2_7b_bf16_stoch", "c4_llama3_70b_bf16_greedy",
                                   "c4_llama3_70b_bf16_t0.7", "c5_ragged_b64_bf16_stoch"])
-def test_configs_full_size(ts, cuda_device, name):
+def test_configs_full_size(ts, cuda_device, name, mode):
     w = gen.get(name)
     x = gi.make_inputs(w, with_attention=False)
-    res = run(ts, x, cuda_device)
+    res = run(ts, x, cuda_device, mode)
     n, ties, flipped = compare_accept(res, x.target_logits, x.draft_tokens, x.draft_probs, x.tree_parents,
                                       x.uniforms, x.temperature)
     print(f"{name}: {n} sequences, {ties} with a rounding tie, {flipped} took the other side")
@@ -67,63 +68,79 @@ def _small(B, N, V, parents, temperature, seed, tied=False, dup=False):
     return logits, tokens, q, parents, u
 
 
-def _run_small(ts, device, logits, tokens, q, parents, u, T):
+def _run_small(ts, device, logits, tokens, q, parents, u, T, mode=0):
     res = ts.tree_accept(dev_tensor(logits, device), dev_tensor(tokens, device),
                          None if q is None else dev_tensor(q, device), dev_tensor(parents, device),
-                         None if u is None else dev_tensor(u, device), T)
+                         None if u is None else dev_tensor(u, device), T, mode=mode)
     torch.cuda.synchronize()
     return compare_accept(res, logits, tokens, q, parents, u, T)
 
 
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("T", [0.0, 1.0, 0.05, 20.0])
 @pytest.mark.parametrize("shape", ["root_only", "chain64", "star64", "random64", "mtp"])
-@pytest.mark.parametrize("V", [7, 256, 5003])
-def test_edge_shapes(ts, cuda_device, T, shape, V):
+@pytest.mark.parametrize("V", [7, 256, 5003, 40000])
+def test_edge_shapes(ts, cuda_device, T, shape, V, mode):
     rng = np.random.default_rng(V)
     parents = {"root_only": [-1], "chain64": trees.chain(64), "star64": trees.star(64),
                "random64": trees.random_recursive(rng, 64), "mtp": [-1, 0]}[shape]
     N = len(parents)
-    data = _small(16, N, V, parents, T, seed=V + N)
-    n, ties, flipped = _run_small(ts, cuda_device, *data, T)
+    data = _small(16 if V < 40000 else 4, N, V, parents, T, seed=V + N)
+    n, ties, flipped = _run_small(ts, cuda_device, *data, T, mode)
     assert flipped <= 1
 
 
-def test_greedy_ties_take_lowest_id(ts, cuda_device):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_greedy_ties_take_lowest_id(ts, cuda_device, mode):
     data = _small(64, 16, 64, trees.random_recursive(np.random.default_rng(1), 16), 0.0, seed=3, tied=True)
-    _run_small(ts, cuda_device, *data, 0.0)
+    _run_small(ts, cuda_device, *data, 0.0, mode)
 
 
-def test_duplicate_sibling_tokens(ts, cuda_device):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_duplicate_sibling_tokens(ts, cuda_device, mode):
     parents = [-1, 0, 0, 0, 1, 2, 3]
     data = _small(256, 7, 300, parents, 1.0, seed=4, dup=True)
-    _run_small(ts, cuda_device, *data, 1.0)
+    _run_small(ts, cuda_device, *data, 1.0, mode)
 
 
-def test_zero_draft_probability(ts, cuda_device):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_zero_draft_probability(ts, cuda_device, mode):
     logits, tokens, q, parents, u = _small(64, 5, 64, [-1, 0, 0, 1, 1], 1.0, seed=5)
     q[:, :, ::2] = 0.0
     q /= q.sum(-1, keepdims=True)
-    _run_small(ts, cuda_device, logits, tokens, q, parents, u, 1.0)
+    _run_small(ts, cuda_device, logits, tokens, q, parents, u, 1.0, mode)
 
 
-def test_bad_tokens_are_flagged(ts, cuda_device):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_bad_tokens_are_flagged(ts, cuda_device, mode):
     logits, tokens, q, parents, u = _small(4, 5, 64, [-1, 0, 0, 1, 1], 0.0, seed=6)
     tokens[0, 1] = 64
     tokens[1, 2] = -3
     ws = torch.empty(ts.accept_workspace_bytes(4, 5, 64), dtype=torch.uint8, device=cuda_device)
     ts.tree_accept(dev_tensor(logits, cuda_device), dev_tensor(tokens, cuda_device), None,
-                   dev_tensor(parents, cuda_device), None, 0.0, workspace=ws)
+                   dev_tensor(parents, cuda_device), None, 0.0, mode=mode, workspace=ws)
     assert ts.read_status(ws) & 8
 
 
-def test_monte_carlo_invariance_on_gpu(ts, cuda_device):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_bad_parents_are_flagged(ts, cuda_device, mode):
+    logits, tokens, q, parents, u = _small(4, 5, 64, [-1, 0, 0, 1, 1], 0.0, seed=7)
+    parents[2, 3] = 4
+    ws = torch.empty(ts.accept_workspace_bytes(4, 5, 64), dtype=torch.uint8, device=cuda_device)
+    ts.tree_accept(dev_tensor(logits, cuda_device), dev_tensor(tokens, cuda_device), None,
+                   dev_tensor(parents, cuda_device), None, 0.0, mode=mode, workspace=ws)
+    assert ts.read_status(ws) & 1
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_monte_carlo_invariance_on_gpu(ts, cuda_device, mode):
     """2^20 trials of the vocab-8 tree: emitted tokens follow p_root then p(. | first)."""
     tables = mc.mc_tables(11)
     trials = 1 << 20
     logits, q, tokens, uniforms, parents = mc.mc_trials(tables, trials, 12)
     path, length, bonus = ts.tree_accept(dev_tensor(logits, cuda_device), dev_tensor(tokens, cuda_device),
                                          dev_tensor(q, cuda_device), dev_tensor(parents, cuda_device),
-                                         dev_tensor(uniforms, cuda_device), 1.0)
+                                         dev_tensor(uniforms, cuda_device), 1.0, mode=mode)
     path, length, bonus = path.cpu().numpy(), length.cpu().numpy(), bonus.cpu().numpy()
     rows = np.arange(trials)
     first = np.where(length >= 1, tokens[rows, path[:, 0].clip(0)], bonus)
