@@ -142,6 +142,30 @@ int tree_attn_verify(const void *q, const void *k_pages, const void *v_pages,
                      const treespec_attn_shape *shape,
                      void *workspace, size_t workspace_bytes, treespec_stream_t stream);
 
+/*
+ * tree_attn_verify_noalloc -- tree_attn_verify without a caller-provided workspace.
+ *
+ * The method's description has no counterpart to this call; it exists for callers
+ * that cannot allocate device memory where they verify a tree (an application that
+ * reserves nearly all device memory up front for its own pools, or a decode loop that
+ * cannot afford an allocation's implicit synchronisation).  Arguments, layouts and
+ * results are those of tree_attn_verify; the scratch space lives in one fixed 32 MiB
+ * device array inside the library instead of `workspace`.
+ *   - The array is held on every GPU that loads the library until the process exits.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.  Nothing is allocated.
+ *   - A shape whose treespec_attn_workspace_bytes exceeds 32 MiB is rejected with
+ *     TREESPEC_ERR_WORKSPACE (fewer splits via shape->num_splits shrink it); other
+ *     argument errors are those of tree_attn_verify.
+ *   - All calls on a device share the array: calls whose work overlaps on the GPU race
+ *     and corrupt each other; serialise them (one stream).  The device status word of
+ *     these calls is not exposed -- use tree_attn_verify to read it.
+ */
+int tree_attn_verify_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                             const int32_t *page_table, const int32_t *prefix_lens,
+                             const int32_t *tree_parents, void *out,
+                             const treespec_attn_shape *shape, treespec_stream_t stream);
+
 /* --------------------------------------------------------------------- accept walk */
 
 /* Workspace bytes tree_accept needs (0 if the sizes are invalid). */
