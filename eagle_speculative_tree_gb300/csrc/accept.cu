@@ -32,17 +32,24 @@ namespace treespec {
 
 namespace {
 
-// Softmax probability of one logit, evaluated identically everywhere.
-__device__ __forceinline__ float prob_at(float logit, float inv_t, float M, float invS) {
-    return expf(fmaf(logit, inv_t, -M)) * invS;
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// r_j(v) from p(v), q(v) and Z_1..Z_j.
-__device__ __forceinline__ float residual_at(float pv, float qv, const float* zs, int j) {
+// Softmax probability of one logit, evaluated identically everywhere:
+// p = 2^(logit * c - M2) / S with c = log2(e) / T and M2 = max(logit * c).
+__device__ __forceinline__ float prob_at(float logit, float c, float M2, float invS) {
+    return ex2(fmaf(logit, c, -M2)) * invS;
+}
+
+// r_j(v) from p(v), q(v) and 1/Z_1 .. 1/Z_j (0 marks a zero-mass residual, left unchanged).
+__device__ __forceinline__ float residual_at(float pv, float qv, const float* izs, int j) {
     float r = pv;
     for (int m = 0; m < j; ++m) {
-        const float z = zs[m];
-        if (z > 0.f) r = fmaxf(r - qv, 0.f) / z;
+        const float iz = izs[m];
+        if (iz > 0.f) r = fmaxf(r - qv, 0.f) * iz;
     }
     return r;
 }
@@ -130,14 +137,69 @@ __device__ __forceinline__ void for_each_pair(const float* a, const float* b, in
     }
 }
 
+// Visitors that pass the float4 lane k (0..3) so callers can keep four independent
+// accumulators per thread.
+template <int NT, bool VEC, typename F>
+__device__ __forceinline__ void for_each4(const float* row, int V, F f) {
+    if constexpr (VEC) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 2
+        for (int v4 = threadIdx.x; v4 < V / 4; v4 += NT) {
+            const float4 x = __ldg(r4 + v4);
+            f(0, x.x);
+            f(1, x.y);
+            f(2, x.z);
+            f(3, x.w);
+        }
+    } else {
+        for (int v = threadIdx.x; v < V; v += NT) f(v & 3, __ldg(row + v));
+    }
+}
+
+template <int NT, bool VEC, typename F>
+__device__ __forceinline__ void for_each_pair4(const float* a, const float* b, int V, F f) {
+    if constexpr (VEC) {
+        const float4* a4 = reinterpret_cast<const float4*>(a);
+        const float4* b4 = reinterpret_cast<const float4*>(b);
+#pragma unroll 2
+        for (int v4 = threadIdx.x; v4 < V / 4; v4 += NT) {
+            const float4 x = __ldg(a4 + v4), y = __ldg(b4 + v4);
+            f(0, x.x, y.x);
+            f(1, x.y, y.y);
+            f(2, x.z, y.z);
+            f(3, x.w, y.w);
+        }
+    } else {
+        for (int v = threadIdx.x; v < V; v += NT) f(v & 3, __ldg(a + v), __ldg(b + v));
+    }
+}
+
 // Lowest index of the row maximum (broadcast to every thread).
 template <int NT, bool VEC>
 __device__ int row_argmax(const float* lg, int V, float* redf, int* redi) {
-    float best = -INFINITY;
-    int bi = 0x7fffffff;
-    for_each<NT, VEC>(lg, V, [&](int v, float x) {
-        if (x > best) { best = x; bi = v; }           // ascending v per thread: keeps the first
-    });
+    float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    int bix[4] = {0x7fffffff, 0x7fffffff, 0x7fffffff, 0x7fffffff};
+    if constexpr (VEC) {
+        const float4* r4 = reinterpret_cast<const float4*>(lg);
+#pragma unroll 2
+        for (int v4 = threadIdx.x; v4 < V / 4; v4 += NT) {     // ascending v per lane: keeps the first
+            const float4 x = __ldg(r4 + v4);
+            if (x.x > bv[0]) { bv[0] = x.x; bix[0] = 4 * v4; }
+            if (x.y > bv[1]) { bv[1] = x.y; bix[1] = 4 * v4 + 1; }
+            if (x.z > bv[2]) { bv[2] = x.z; bix[2] = 4 * v4 + 2; }
+            if (x.w > bv[3]) { bv[3] = x.w; bix[3] = 4 * v4 + 3; }
+        }
+    } else {
+        for (int v = threadIdx.x; v < V; v += NT) {
+            const float x = __ldg(lg + v);
+            if (x > bv[0]) { bv[0] = x; bix[0] = v; }
+        }
+    }
+    float best = bv[0];
+    int bi = bix[0];
+#pragma unroll
+    for (int k = 1; k < 4; ++k)
+        if (bv[k] > best || (bv[k] == best && bix[k] < bi)) { best = bv[k]; bi = bix[k]; }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float ob = __shfl_xor_sync(0xffffffffu, best, o);
@@ -157,137 +219,141 @@ __device__ int row_argmax(const float* lg, int V, float* redf, int* redi) {
     return redi[0];
 }
 
-// (M, S): M = max(logits / T), S = sum exp(logits / T - M) (broadcast).
+// (M2, S): M2 = max(logits * c), S = sum 2^(logits * c - M2) with c = log2(e) / T
+// (broadcast).  Two passes over the row: the second one hits L2.
 template <int NT, bool VEC>
-__device__ float2 row_softmax_stats(const float* lg, int V, float inv_t, float* redf, double* redd) {
-    float m = -INFINITY;
-    KSum s;
-    for_each<NT, VEC>(lg, V, [&](int, float x) {
-        const float y = x * inv_t;
-        if (y > m) {
-            const float a = expf(m - y);
-            s.s *= a;
-            s.c *= a;
-            m = y;
-        }
-        s.add(expf(y - m));
-    });
-    const float M = block_max_f<NT>(m, redf);
-    const double part = (m == -INFINITY) ? 0.0 : s.value() * double(expf(m - M));
-    const double S = block_sum_d<NT>(part, redd);
-    return make_float2(M, float(S));
+__device__ float2 row_softmax_stats(const float* lg, int V, float c, float* redf, double* redd) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for_each4<NT, VEC>(lg, V, [&](int k, float x) { m[k] = fmaxf(m[k], x); });
+    const float mx = block_max_f<NT>(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), redf);
+    const float M2 = mx * c;                     // c > 0 commutes with max
+    KSum s[4];
+    for_each4<NT, VEC>(lg, V, [&](int k, float x) { s[k].add(ex2(fmaf(x, c, -M2))); });
+    const double S = block_sum_d<NT>((s[0].value() + s[1].value()) + (s[2].value() + s[3].value()), redd);
+    return make_float2(M2, float(S));
 }
 
 // Z_{j+1} = sum_v max(0, r_j(v) - q(v)) for the row (broadcast).
 template <int NT, bool VEC>
-__device__ float row_residual_mass(const float* lg, const float* qr, int V, float inv_t, float M, float invS,
-                                   const float* zs, int j, double* redd) {
-    KSum z;
-    for_each_pair<NT, VEC>(lg, qr, V, [&](float x, float qv) {
-        z.add(fmaxf(residual_at(prob_at(x, inv_t, M, invS), qv, zs, j) - qv, 0.f));
+__device__ float row_residual_mass(const float* lg, const float* qr, int V, float c, float M2, float invS,
+                                   const float* izs, int j, double* redd) {
+    KSum z[4];
+    for_each_pair4<NT, VEC>(lg, qr, V, [&](int k, float x, float qv) {
+        z[k].add(fmaxf(residual_at(prob_at(x, c, M2, invS), qv, izs, j) - qv, 0.f));
     });
-    return float(block_sum_d<NT>(z.value(), redd));
+    return float(block_sum_d<NT>((z[0].value() + z[1].value()) + (z[2].value() + z[3].value()), redd));
 }
 
 // Term of the bonus distribution at token v: r_rej(v) up to normalisation.
 struct BonusTerm {
     const float* lg;
     const float* qr;
-    const float* zs;
-    float inv_t, M, invS;
+    const float* izs;
+    float c, M2, invS;
     int rej;          // number of rejected children at the final node
     bool unchanged;   // the last residual had zero mass: use r_{rej-1} itself
     __device__ __forceinline__ float operator()(int v) const {
-        const float pv = prob_at(__ldg(lg + v), inv_t, M, invS);
+        const float pv = prob_at(__ldg(lg + v), c, M2, invS);
         if (rej == 0) return pv;
         const float qv = __ldg(qr + v);
-        const float r = residual_at(pv, qv, zs, rej - 1);
+        const float r = residual_at(pv, qv, izs, rej - 1);
         return unchanged ? r : fmaxf(r - qv, 0.f);
     }
 };
 
+__device__ __forceinline__ double warp_inclusive_scan_d(double x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
 // Smallest v with sum_{w <= v} term(w) > u0 * sum_w term(w) (whole CTA; broadcast).
+// Pass 1: the warps sum segments of `seg_len` tokens (float64 per segment).  Then warp 0
+// scans the segment sums in order to find the segment holding the threshold and scans
+// that segment 32 tokens at a time.  A threshold at or above the total (rounding)
+// yields the largest token with mass; a residual with no mass falls back to r_{rej-1}.
 template <int NT>
 __device__ int bonus_scan(BonusTerm term, int V, float u0) {
     constexpr int NW = NT / 32;
-    __shared__ double segsum[NW];
-    __shared__ double s_base, s_thr;
-    __shared__ int s_seg, s_found, s_unchanged;
-    __shared__ int lastnz[NW];
+    constexpr int kMaxSeg = 2048;
+    __shared__ double segsum[kMaxSeg];
+    __shared__ int s_state, s_result;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int seg = ((V + NW - 1) / NW + 31) / 32 * 32;
-    const int s0 = warp * seg, s1 = min(V, s0 + seg);
-    __syncthreads();
-    if (threadIdx.x == 0) s_unchanged = 0;
-    __syncthreads();
+    int seg_len = 512;
+    while ((V + seg_len - 1) / seg_len > kMaxSeg) seg_len *= 2;
+    const int nseg = (V + seg_len - 1) / seg_len;
     for (int attempt = 0; attempt < 2; ++attempt) {
-        term.unchanged = s_unchanged != 0;
-        double part = 0.0;
-        for (int v = s0 + lane; v < s1; v += 32) part += double(term(v));
-        part = warp_sum_d(part);
-        if (lane == 0) segsum[warp] = part;
+        term.unchanged = attempt == 1;
+        for (int sg = warp; sg < nseg; sg += NW) {
+            const int a = sg * seg_len, e = min(V, a + seg_len);
+            double part = 0.0;
+            for (int v = a + lane; v < e; v += 32) part += double(term(v));
+            part = warp_sum_d(part);
+            if (lane == 0) segsum[sg] = part;
+        }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (warp == 0) {
             double total = 0.0;
-            for (int w = 0; w < NW; ++w) total += segsum[w];
-            s_found = 0;
+            for (int k0 = 0; k0 < nseg; k0 += 32) total += warp_sum_d(k0 + lane < nseg ? segsum[k0 + lane] : 0.0);
+            int state = 1, result = -1;
             if (total > 0.0) {
                 const double thr = double(u0) * total;
-                double pre = 0.0;
-                s_seg = -1;
-                for (int w = 0; w < NW; ++w) {
-                    if (pre + segsum[w] > thr) { s_seg = w; break; }
-                    pre += segsum[w];
+                double run = 0.0;
+                int hit = -1;
+                for (int k0 = 0; k0 < nseg && hit < 0; k0 += 32) {
+                    const double x = k0 + lane < nseg ? segsum[k0 + lane] : 0.0;
+                    const double inc = warp_inclusive_scan_d(x);
+                    const unsigned hb = __ballot_sync(0xffffffffu, run + inc > thr);
+                    if (hb) {
+                        const int l = __ffs(hb) - 1;
+                        hit = k0 + l;
+                        run += __shfl_sync(0xffffffffu, inc - x, l);
+                    } else {
+                        run += __shfl_sync(0xffffffffu, inc, 31);
+                    }
                 }
-                s_base = pre;
-                s_thr = thr;
-                s_found = 1;
-            } else if (term.rej > 0 && !s_unchanged) {
-                s_unchanged = 1;          // zero residual mass: the distribution stays r_{rej-1}
-                s_found = 2;
+                if (hit >= 0) {
+                    const int a = hit * seg_len, e = min(V, a + seg_len);
+                    int last_nz = -1;
+                    for (int v0 = a; v0 < e; v0 += 32) {
+                        const int v = v0 + lane;
+                        const double x = v < e ? double(term(v)) : 0.0;
+                        const double inc = warp_inclusive_scan_d(x);
+                        const unsigned hb = __ballot_sync(0xffffffffu, run + inc > thr);
+                        const unsigned nz = __ballot_sync(0xffffffffu, x > 0.0);
+                        if (nz) last_nz = v0 + 31 - __clz(nz);
+                        if (hb) { result = v0 + __ffs(hb) - 1; break; }
+                        run += __shfl_sync(0xffffffffu, inc, 31);
+                    }
+                    if (result < 0) result = last_nz;        // rounding between the two passes
+                } else {
+                    for (int sg = nseg - 1; sg >= 0 && result < 0; --sg) {
+                        if (!(segsum[sg] > 0.0)) continue;
+                        const int a = sg * seg_len, e = min(V, a + seg_len);
+                        int ln = -1;
+                        for (int v = a + lane; v < e; v += 32)
+                            if (term(v) > 0.f) ln = v;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) ln = max(ln, __shfl_xor_sync(0xffffffffu, ln, o));
+                        result = ln;
+                    }
+                }
+            } else if (term.rej > 0 && attempt == 0) {
+                state = 2;                                 // zero residual mass: keep r_{rej-1}
+            }
+            if (lane == 0) {
+                s_state = state;
+                s_result = result;
             }
         }
         __syncthreads();
-        if (s_found != 2) break;
+        if (s_state != 2) break;
     }
-    const int sel = (s_found == 1) ? s_seg : -1;
-    if (sel >= 0 && warp == sel) {
-        double run = s_base;
-        const double thr = s_thr;
-        int v_hit = -1, last_nz = -1;
-        for (int v0 = s0; v0 < s1; v0 += 32) {
-            const int v = v0 + lane;
-            const double x = v < s1 ? double(term(v)) : 0.0;
-            double inc = x;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, run + inc > thr);
-            const unsigned nz = __ballot_sync(0xffffffffu, x > 0.0);
-            if (nz) last_nz = v0 + 31 - __clz(nz);
-            if (hit) { v_hit = v0 + __ffs(hit) - 1; break; }
-            run += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        if (v_hit < 0) v_hit = last_nz;        // rounding between the two passes
-        if (lane == 0) lastnz[0] = v_hit;
-    }
-    if (sel < 0) {                             // threshold at or above the total by rounding
-        int ln = -1;
-        for (int v = s0 + lane; v < s1; v += 32)
-            if (term(v) > 0.f) ln = v;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ln = max(ln, __shfl_xor_sync(0xffffffffu, ln, o));
-        if (lane == 0) lastnz[warp] = ln;
-    }
-    __syncthreads();
-    int v = -1;
-    if (sel >= 0) {
-        v = lastnz[0];
-    } else {
-        for (int w = 0; w < NW; ++w) v = max(v, lastnz[w]);
-    }
+    const int v = s_result;
     __syncthreads();
     return v < 0 ? 0 : v;
 }
@@ -306,7 +372,7 @@ __global__ void __launch_bounds__(NT) accept_rows_kernel(AcceptParams p) {
     __shared__ double redd[32];
     __shared__ float redf[32];
     __shared__ int redi[32];
-    __shared__ float zsm[kMaxNodes];
+    __shared__ float izs[kMaxNodes];
     const int row = blockIdx.x;                 // b * N + i
     const int b = row / p.N, i = row % p.N;
     const float* lg = p.logits + size_t(row) * p.V;
@@ -314,7 +380,7 @@ __global__ void __launch_bounds__(NT) accept_rows_kernel(AcceptParams p) {
         const int a = row_argmax<NT, VEC>(lg, p.V, redf, redi);
         if (threadIdx.x == 0) p.amax[row] = a;
     } else {
-        const float2 st = row_softmax_stats<NT, VEC>(lg, p.V, p.inv_t, redf, redd);
+        const float2 st = row_softmax_stats<NT, VEC>(lg, p.V, p.c, redf, redd);
         const float invS = 1.f / st.y;
         if (threadIdx.x == 0) {
             p.stats[size_t(row) * 2] = st.x;
@@ -324,10 +390,11 @@ __global__ void __launch_bounds__(NT) accept_rows_kernel(AcceptParams p) {
         for (int c = i + 1; c < p.N; ++c) k += (p.parents[size_t(b) * p.N + c] == i);
         const float* qr = p.probs + size_t(row) * p.V;
         for (int j = 1; j < k; ++j) {                // Z_1 .. Z_{k-1}
-            const float Z = row_residual_mass<NT, VEC>(lg, qr, p.V, p.inv_t, st.x, invS, zsm, j - 1, redd);
+            const float Z = row_residual_mass<NT, VEC>(lg, qr, p.V, p.c, st.x, invS, izs, j - 1, redd);
             if (threadIdx.x == 0) {
-                zsm[j - 1] = Z;
-                p.zs[size_t(row) * kMaxNodes + (j - 1)] = Z;
+                const float iz = Z > 0.f ? 1.f / Z : 0.f;
+                izs[j - 1] = iz;
+                p.izs[size_t(row) * kMaxNodes + (j - 1)] = iz;
             }
             __syncthreads();
         }
@@ -337,7 +404,7 @@ __global__ void __launch_bounds__(NT) accept_rows_kernel(AcceptParams p) {
 template <int NT, bool STOCH>
 __global__ void __launch_bounds__(NT) accept_walk_kernel(AcceptParams p) {
     __shared__ int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
-    __shared__ float zsm[kMaxNodes];
+    __shared__ float izs[kMaxNodes];
     __shared__ int s_cur, s_rej, s_len;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int N = p.N, V = p.V;
@@ -352,10 +419,10 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(AcceptParams p) {
         for (;;) {
             const size_t row = size_t(b) * N + cur;
             int accepted = -1, jj = 0;
-            float M = 0.f, invS = 0.f;
-            const float* zs = p.zs + row * kMaxNodes;
+            float M2 = 0.f, invS = 0.f;
+            const float* rz = p.izs + row * kMaxNodes;
             if (STOCH) {
-                M = p.stats[row * 2];
+                M2 = p.stats[row * 2];
                 invS = 1.f / p.stats[row * 2 + 1];
             }
             for (int c = cur + 1; c < N; ++c) {
@@ -369,7 +436,7 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(AcceptParams p) {
                         ok = (x == p.amax[row]);
                     } else {
                         const float qx = p.probs[row * V + x];
-                        const float r = residual_at(prob_at(p.logits[row * V + x], p.inv_t, M, invS), qx, zs, jj);
+                        const float r = residual_at(prob_at(p.logits[row * V + x], p.c, M2, invS), qx, rz, jj);
                         ok = r > 0.f && p.uniforms[size_t(b) * N + c] * qx <= r;
                     }
                 }
@@ -392,9 +459,9 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(AcceptParams p) {
     if constexpr (STOCH) {
         const size_t row = size_t(b) * N + s_cur;
         const int rej = s_rej;
-        for (int t = tid; t < kMaxNodes; t += NT) zsm[t] = (t < rej) ? p.zs[row * kMaxNodes + t] : 0.f;
+        for (int t = tid; t < kMaxNodes; t += NT) izs[t] = (t < rej) ? p.izs[row * kMaxNodes + t] : 0.f;
         __syncthreads();
-        const BonusTerm term{p.logits + row * V, p.probs + row * V, zsm, p.inv_t, p.stats[row * 2],
+        const BonusTerm term{p.logits + row * V, p.probs + row * V, izs, p.c, p.stats[row * 2],
                              1.f / p.stats[row * 2 + 1], rej, false};
         const int v = bonus_scan<NT>(term, V, p.uniforms[size_t(b) * N]);
         if (tid == 0) p.bonus[b] = v;
@@ -406,7 +473,7 @@ __global__ void __launch_bounds__(NT) accept_walk_kernel(AcceptParams p) {
 template <int NT, bool VEC, bool STOCH>
 __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
     __shared__ int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
-    __shared__ float zsm[kMaxNodes];
+    __shared__ float izs[kMaxNodes];
     __shared__ double redd[32];
     __shared__ float redf[32];
     __shared__ int redi[32];
@@ -426,7 +493,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
     }
     __syncthreads();
     int amax = 0, rej = 0;
-    float M = 0.f, invS = 1.f;
+    float M2 = 0.f, invS = 1.f;
     for (int depth = 0; depth < N; ++depth) {
         const int cur = s_cur;
         const size_t row = size_t(b) * N + cur;
@@ -435,8 +502,8 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
         if constexpr (!STOCH) {
             amax = row_argmax<NT, VEC>(lg, V, redf, redi);
         } else {
-            const float2 sm = row_softmax_stats<NT, VEC>(lg, V, p.inv_t, redf, redd);
-            M = sm.x;
+            const float2 sm = row_softmax_stats<NT, VEC>(lg, V, p.c, redf, redd);
+            M2 = sm.x;
             invS = 1.f / sm.y;
         }
         // try the children of cur in ascending node index
@@ -457,7 +524,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
                             ok = x == amax;
                         } else {
                             const float qx = qr[x];
-                            const float r = residual_at(prob_at(lg[x], p.inv_t, M, invS), qx, zsm, jj);
+                            const float r = residual_at(prob_at(lg[x], p.c, M2, invS), qx, izs, jj);
                             ok = r > 0.f && p.uniforms[size_t(b) * N + nc] * qx <= r;
                         }
                     }
@@ -481,8 +548,8 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
             ++jj;
             if (action == 3) break;
             if constexpr (STOCH) {                        // next sibling sees the residual
-                const float Z = row_residual_mass<NT, VEC>(lg, qr, V, p.inv_t, M, invS, zsm, jj - 1, redd);
-                if (tid == 0) zsm[jj - 1] = Z;
+                const float Z = row_residual_mass<NT, VEC>(lg, qr, V, p.c, M2, invS, izs, jj - 1, redd);
+                if (tid == 0) izs[jj - 1] = Z > 0.f ? 1.f / Z : 0.f;
                 __syncthreads();
             }
             pos = child;
@@ -506,7 +573,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
         if (tid == 0) p.bonus[b] = amax;
     } else {
         const size_t row = size_t(b) * N + s_cur;
-        const BonusTerm term{p.logits + row * V, p.probs + row * V, zsm, p.inv_t, M, invS, rej, false};
+        const BonusTerm term{p.logits + row * V, p.probs + row * V, izs, p.c, M2, invS, rej, false};
         const int v = bonus_scan<NT>(term, V, p.uniforms[size_t(b) * N]);
         if (tid == 0) p.bonus[b] = v;
     }

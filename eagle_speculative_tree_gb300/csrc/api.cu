@@ -139,7 +139,7 @@ AcceptLayout accept_layout(int B, int N) {
     off = align_up(off + size_t(B) * N * 4, kWsAlign);
     L.stats = off;
     off = align_up(off + size_t(B) * N * 8, kWsAlign);
-    L.zs = off;
+    L.izs = off;
     off = align_up(off + size_t(B) * N * kMaxNodes * 4, kWsAlign);
     L.total = off;
     return L;
@@ -283,12 +283,12 @@ extern "C" int tree_accept_with_mode(const float* target_logits, const int32_t* 
     p.status = reinterpret_cast<uint32_t*>(ws + lay.status);
     p.amax = reinterpret_cast<int32_t*>(ws + lay.amax);
     p.stats = reinterpret_cast<float*>(ws + lay.stats);
-    p.zs = reinterpret_cast<float*>(ws + lay.zs);
+    p.izs = reinterpret_cast<float*>(ws + lay.izs);
     p.B = batch;
     p.N = num_nodes;
     p.V = vocab;
     p.temperature = temperature;
-    p.inv_t = stoch ? 1.f / temperature : 0.f;
+    p.c = stoch ? float(1.4426950408889634 / double(temperature)) : 0.f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     int kernels = 0;

@@ -3,19 +3,21 @@
 // Same partial state as the CUDA-core kernel (m, l, acc per query row of one split),
 // computed with tcgen05:
 //   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
-//     are zero) x one split of the sequence's logical tokens;
+//     are zero) x one split of the sequence's logical tokens, in 128-token tiles;
 //   * warp 0 streams the split's K and V pages with TMA (one 16-token page x 64
-//     head-dim columns per copy, 128-byte swizzle) into a two-stage ring; the partly
-//     filled last page of a sequence and pages past the split are written by the warp
-//     itself, zero-filled, so nothing outside the sequence reaches the MMA;
-//   * warp 1 allocates TMEM (S double buffer + O) and issues S = Q K^T and O += P V as
-//     128x128x16 tcgen05.mma instructions from shared-memory descriptors;
+//     head-dim columns per copy, 128-byte swizzle) into a three-stage ring, and asks
+//     the L2 for the pages of the tile four steps ahead; the partly filled last page
+//     of a sequence and pages past the split are written by the warp itself,
+//     zero-filled, so nothing outside the sequence reaches the MMA;
+//   * warp 1 allocates all 512 TMEM columns (S and P double-buffered, O) and issues
+//     S = Q K^T from shared memory and O += P V with P read from TMEM, as
+//     128x128x16 tcgen05.mma instructions;
 //   * warps 2-5 (one TMEM lane quarter each, one query row per thread) read S from
 //     TMEM, apply the tree mask -- prefix tokens always, tree token S+j only when bit
 //     j of the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2
 //     mask M and section 5 bitmask) -- run the online softmax in base 2, write P as
-//     bf16 to shared memory, and rescale O in TMEM only when a row's running max grows
-//     by more than 2^8.
+//     packed bf16 back to TMEM, and rescale O in TMEM only when a row's running max
+//     grows by more than 2^8.
 // Every mbarrier wait is bounded; on expiry the CTA records TREESPEC_STATUS_TIMEOUT,
 // drains its own tensor-core work, frees TMEM and exits.
 #include <cuda.h>
@@ -33,26 +35,29 @@ using namespace sm100;
 constexpr int kM = 128;              // query rows per CTA = TMEM lanes
 constexpr int kD = 128;              // head dim
 constexpr int kBN = 128;             // tokens per tile
-constexpr int kNS = 2;               // K/V ring stages
+constexpr int kNS = 3;               // K/V ring stages
+constexpr int kPrefetch = 4;         // tiles of L2 prefetch ahead of the TMA loads
 constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
 constexpr int kTile = 2 * kPanel;    // [128][128] bf16
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;        // S double buffer: columns [0, 256)
+constexpr uint32_t kColP = 256;      // P double buffer (bf16 pairs): [256, 384)
+constexpr uint32_t kColO = 384;      // O: [384, 512)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;
 constexpr int kOffV = kOffK + kNS * kTile;
-constexpr int kOffP = kOffV + kNS * kTile;
-constexpr int kOffBar = kOffP + kTile;
-constexpr int kNumBars = 2 * kNS + 2 + 2 + 4;   // kv_full, kv_empty, s_full, s_empty, p_full, o_done, q_full, drain
+constexpr int kOffBar = kOffV + kNS * kTile;
+constexpr int kNumBars = 2 * kNS + 2 + 2 + 2 + 2 + 2;   // kv_full/empty, s_full/empty, p_full, p_free, q_full, drain
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffAnc = (kOffMisc + 16 + 7) / 8 * 8;
 constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8 + 1024;   // + alignment slack
 
 struct Bars {
-    uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], s_empty[2], p_full, o_done, q_full, drain;
+    uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], s_empty[2], p_full[2], p_free[2], q_full, drain;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -106,9 +111,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
             mbar_init(&bars->s_empty[s], 128);
+            mbar_init(&bars->p_full[s], 128);
+            mbar_init(&bars->p_free[s], 1);
         }
-        mbar_init(&bars->p_full, 128);
-        mbar_init(&bars->o_done, 1);
         mbar_init(&bars->q_full, 128);
         mbar_init(&bars->drain, 1);
         *abort_flag = 0;
@@ -137,11 +142,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos0 = t0 + j * kBN + lane * 16;
             return (lane < 8 && j < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
         };
+        // L2 prefetch of tile j: lane = (page pg = lane / 4, quarter = lane % 4 ->
+        // K or V, first or second 128-byte half of the 256-byte head row)
+        auto prefetch_tile = [&](int j) {
+            const int pg = lane >> 2, part = lane & 3;
+            const int pos0 = t0 + j * kBN + pg * 16;
+            if (j >= ntiles || pos0 >= t1) return;
+            const int page = __ldg(ptab + (pos0 >> 4));
+            if (page < 0 || page >= p.num_pool_pages) return;
+            const unsigned char* base = static_cast<const unsigned char*>((part & 2) ? p.v : p.k) +
+                                        (size_t(page) * p.ps * p.Hkv + h) * (kD * 2) + (part & 1) * 128;
+            const int nrows = min(16, t1 - pos0);
+            for (int r = 0; r < nrows; ++r) prefetch_l2(base + size_t(r) * p.Hkv * (kD * 2));
+        };
+        for (int j = 0; j < kPrefetch; ++j) prefetch_tile(j);
         int page_next = fetch_pages(0);
         for (int j = 0; j < ntiles; ++j) {
             const int stage = j % kNS;
             int page = page_next;
             page_next = fetch_pages(j + 1);
+            prefetch_tile(j + kPrefetch);
             if (j >= kNS && !mbar_wait_bounded(&bars->kv_empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
@@ -203,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
-            const uint32_t qaddr = sbase + kOffQ, paddr = sbase + kOffP;
+            const uint32_t qaddr = sbase + kOffQ;
             bool ok = mbar_wait_bounded(&bars->q_full, 0, kWaitNs);
             auto issue_s = [&](int j) -> bool {
                 const int stage = j % kNS;
@@ -211,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j >= 2 && !mbar_wait_bounded(&bars->s_empty[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) return false;
                 tc_fence_after();
                 const uint32_t kaddr = sbase + kOffK + stage * kTile;
-                const uint32_t d = tbase + uint32_t(j & 1) * 128u;
+                const uint32_t d = tbase + kColS + uint32_t(j & 1) * 128u;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t koff = (kk >> 2) * kPanel + (kk & 3) * 32;
@@ -222,18 +242,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait_bounded(&bars->p_full, j & 1, kWaitNs)) return false;
+                if (!mbar_wait_bounded(&bars->p_full[j & 1], (j >> 1) & 1, kWaitNs)) return false;
                 tc_fence_after();
                 const int stage = j % kNS;
                 const uint32_t vaddr = sbase + kOffV + stage * kTile;
+                const uint32_t pcol = tbase + kColP + uint32_t(j & 1) * 64u;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint32_t poff = (kk >> 2) * kPanel + (kk & 3) * 32;
-                    mma_bf16_ss(tbase + 256u, smem_desc(paddr + poff, 16, 1024),
-                                smem_desc(vaddr + kk * 2048, kPanel, 1024), kIdO, (j > 0 || kk > 0));
+                for (int kk = 0; kk < kBN / 16; ++kk) {      // 16 tokens = 8 packed columns of P
+                    mma_bf16_ts(tbase + kColO, pcol + kk * 8, smem_desc(vaddr + kk * 2048, kPanel, 1024), kIdO,
+                                (j > 0 || kk > 0));
                 }
                 mma_commit(&bars->kv_empty[stage]);
-                mma_commit(&bars->o_done);
+                mma_commit(&bars->p_free[j & 1]);
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -305,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t v[kBN];
             if (warp_rows) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tl + uint32_t(j & 1) * 128u + c * 32, v + c * 32);
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + kColS + uint32_t(j & 1) * 128u + c * 32, v + c * 32);
                 tmem_wait_ld();
             }
             tc_fence_before();
@@ -342,43 +362,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l += lsum;
-            // P buffer and O are free once P_{j-1} V_{j-1} has completed
-            if (j > 0 && !mbar_wait_bounded(&bars->o_done, (j - 1) & 1, kWaitNs)) { alive = false; break; }
-            tc_fence_after();
+            // P buffer j&1 is free once P_{j-2} V_{j-2} has completed
+            if (j >= 2 && !mbar_wait_bounded(&bars->p_free[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) {
+                alive = false;
+                break;
+            }
             if (__any_sync(0xffffffffu, resc)) {
+                // O may only be rescaled once P_{j-1} V_{j-1} is in it
+                if (!mbar_wait_bounded(&bars->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitNs)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
                 const float f = resc ? alpha : 1.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tl + 256u + c * 32, o);
+                    tmem_ld32(tl + kColO + c * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st32(tl + 256u + c * 32, o);
+                    tmem_st32(tl + kColO + c * 32, o);
                 }
-                tmem_wait_st();
             }
-            if (row_ok) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<uint4*>(sm + kOffP + (c >> 3) * kPanel + sw128_offset(t, c & 7)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            tc_fence_after();
+            if (warp_rows) {
+                tmem_st32(tl + kColP + uint32_t(j & 1) * 64u, pk);
+                tmem_st32(tl + kColP + uint32_t(j & 1) * 64u + 32u, pk + 32);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->p_full);
+            mbar_arrive(&bars->p_full[j & 1]);
         }
         if (!alive) {
             *abort_flag = 1;
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-        } else if (mbar_wait_bounded(&bars->o_done, (ntiles - 1) & 1, kWaitNs)) {
+        } else if (mbar_wait_bounded(&bars->p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, kWaitNs)) {
             tc_fence_after();
             const float inv = 1.f / l;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 if (warp_rows) {
-                    tmem_ld32(tl + 256u + c * 32, o);
+                    tmem_ld32(tl + kColO + c * 32, o);
                     tmem_wait_ld();
                 }
                 if (!row_ok) continue;

@@ -77,7 +77,7 @@ struct AttnParams {
 // ------------------------------------------------------------------ accept
 
 struct AcceptLayout {
-    size_t status, amax, stats, zs, total;
+    size_t status, amax, stats, izs, total;
 };
 
 struct AcceptParams {
@@ -91,11 +91,11 @@ struct AcceptParams {
     int32_t* bonus;
     uint32_t* status;
     int32_t* amax;    // [B][N]   lowest argmax of each target row
-    float* stats;     // [B][N][2] (M, S): max of logits/T and sum of exp(logits/T - M)
-    float* zs;        // [B][N][64] Z_1.. of the sibling residual chain of each row
+    float* stats;     // [B][N][2] (M2, S): max of logits*c and sum of 2^(logits*c - M2)
+    float* izs;       // [B][N][64] 1/Z_1.. of the sibling residual chain of each row (0: Z = 0)
     int B, N, V;
     float temperature;
-    float inv_t;
+    float c;          // log2(e) / temperature
 };
 
 // Kernel launchers (each returns cudaGetLastError() of its launch).
