@@ -5,10 +5,10 @@
 //   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
 //     are zero) x one split of the sequence's logical tokens, in 128-token tiles;
 //   * warp 0 streams the split's K and V pages with TMA (one 16-token page x 64
-//     head-dim columns per copy, 128-byte swizzle) into a three-stage ring, and asks
-//     the L2 for the pages of the tile four steps ahead; the partly filled last page
-//     of a sequence and pages past the split are written by the warp itself,
-//     zero-filled, so nothing outside the sequence reaches the MMA;
+//     head-dim columns per copy, 128-byte swizzle; lanes 0-7 issue one page each)
+//     into a three-stage ring; the partly filled last page of a sequence and pages
+//     past the split are written by the warp itself, zero-filled, so nothing outside
+//     the sequence reaches the MMA;
 //   * warp 1 allocates all 512 TMEM columns (S and P double-buffered, O) and issues
 //     S = Q K^T from shared memory and O += P V with P read from TMEM, as
 //     128x128x16 tcgen05.mma instructions;
@@ -36,7 +36,6 @@ constexpr int kM = 128;              // query rows per CTA = TMEM lanes
 constexpr int kD = 128;              // head dim
 constexpr int kBN = 128;             // tokens per tile
 constexpr int kNS = 3;               // K/V ring stages
-constexpr int kPrefetch = 4;         // tiles of L2 prefetch ahead of the TMA loads
 constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
 constexpr int kTile = 2 * kPanel;    // [128][128] bf16
 constexpr int kThreads = 192;
@@ -142,79 +141,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos0 = t0 + j * kBN + lane * 16;
             return (lane < 8 && j < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
         };
-        // L2 prefetch of tile j: lane = (page pg = lane / 4, quarter = lane % 4 ->
-        // K or V, first or second 128-byte half of the 256-byte head row)
-        auto prefetch_tile = [&](int j) {
-            const int pg = lane >> 2, part = lane & 3;
-            const int pos0 = t0 + j * kBN + pg * 16;
-            if (j >= ntiles || pos0 >= t1) return;
-            const int page = __ldg(ptab + (pos0 >> 4));
-            if (page < 0 || page >= p.num_pool_pages) return;
-            const unsigned char* base = static_cast<const unsigned char*>((part & 2) ? p.v : p.k) +
-                                        (size_t(page) * p.ps * p.Hkv + h) * (kD * 2) + (part & 1) * 128;
-            const int nrows = min(16, t1 - pos0);
-            for (int r = 0; r < nrows; ++r) prefetch_l2(base + size_t(r) * p.Hkv * (kD * 2));
-        };
-        for (int j = 0; j < kPrefetch; ++j) prefetch_tile(j);
         int page_next = fetch_pages(0);
         for (int j = 0; j < ntiles; ++j) {
             const int stage = j % kNS;
             int page = page_next;
             page_next = fetch_pages(j + 1);
-            prefetch_tile(j + kPrefetch);
             if (j >= kNS && !mbar_wait_bounded(&bars->kv_empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
             }
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             const int base = t0 + j * kBN;
-            // classify the tile's 8 pages: 1 = TMA, 2 = written here (partial / bad / absent)
-            int kind = 2;
+            // lanes 0..7 own page `lane` of the tile: 1 = full page by TMA, 2 = written here
+            // (the sequence's partly filled last page, a bad page id, or past the split)
+            const int pos0 = base + lane * 16;
+            int kind = 0;
             if (lane < 8) {
-                const int pos0 = base + lane * 16;
+                kind = 2;
                 if (pos0 < t1) {
                     const bool ok = page >= 0 && page < p.num_pool_pages;
                     if (!ok) atomicOr(p.status, TREESPEC_STATUS_BAD_PAGE);
-                    kind = (ok && pos0 + 16 <= L) ? 1 : 2;
+                    if (ok && pos0 + 16 <= L) kind = 1;
                     if (!ok) page = -1;
+                } else {
+                    page = -1;
                 }
             }
             unsigned char* Ks = sm + kOffK + stage * kTile;
             unsigned char* Vs = sm + kOffV + stage * kTile;
-            const unsigned manual = __ballot_sync(0xffffffffu, lane < 8 && kind == 2);
-            for (int pg = 0; pg < 8; ++pg) {
-                if (!((manual >> pg) & 1u)) continue;
-                const int pgid = __shfl_sync(0xffffffffu, page, pg);
-                const int pos0 = base + pg * 16;
-                for (int c = lane; c < 16 * 16; c += 32) {      // 16 token rows x 16 chunks of 16 bytes
-                    const int rr = c >> 4, ch = c & 15;
-                    const int pos = pos0 + rr;
-                    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-                    if (pgid >= 0 && pos < t1) {
-                        const size_t off = ((size_t(pgid) * p.ps + (pos & 15)) * p.Hkv + h) * kD + ch * 8;
-                        kv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k) + off));
-                        vv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v) + off));
+            const unsigned manual = __ballot_sync(0xffffffffu, kind == 2);
+            if (manual) {
+                for (int pg = 0; pg < 8; ++pg) {
+                    if (!((manual >> pg) & 1u)) continue;
+                    const int pgid = __shfl_sync(0xffffffffu, page, pg);
+                    const int q0 = base + pg * 16;
+                    for (int c = lane; c < 16 * 16; c += 32) {      // 16 token rows x 16 chunks of 16 bytes
+                        const int rr = c >> 4, ch = c & 15;
+                        const int pos = q0 + rr;
+                        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+                        if (pgid >= 0 && pos < t1) {
+                            const size_t off = ((size_t(pgid) * p.ps + (pos & 15)) * p.Hkv + h) * kD + ch * 8;
+                            kv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k) + off));
+                            vv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v) + off));
+                        }
+                        const uint32_t o = (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7);
+                        *reinterpret_cast<uint4*>(Ks + o) = kv;
+                        *reinterpret_cast<uint4*>(Vs + o) = vv;
                     }
-                    const uint32_t o = (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7);
-                    *reinterpret_cast<uint4*>(Ks + o) = kv;
-                    *reinterpret_cast<uint4*>(Vs + o) = vv;
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
             }
-            fence_proxy_async_smem();
+            const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
+            if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[stage], uint32_t(__popc(viatma)) * 4u * 2048u);
             __syncwarp();
-            const unsigned viatma = __ballot_sync(0xffffffffu, lane < 8 && kind == 1);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars->kv_full[stage], uint32_t(__popc(viatma)) * 4u * 2048u);
-            }
-            for (int pg = 0; pg < 8; ++pg) {
-                const int pgid = __shfl_sync(0xffffffffu, page, pg);
-                if (lane == 0 && ((viatma >> pg) & 1u)) {
-                    const int z = pgid * 16;
-                    tma_load_3d(Ks + pg * 2048, &tmk, 0, h, z, &bars->kv_full[stage]);
-                    tma_load_3d(Ks + kPanel + pg * 2048, &tmk, 64, h, z, &bars->kv_full[stage]);
-                    tma_load_3d(Vs + pg * 2048, &tmv, 0, h, z, &bars->kv_full[stage]);
-                    tma_load_3d(Vs + kPanel + pg * 2048, &tmv, 64, h, z, &bars->kv_full[stage]);
-                }
+            if (kind == 1) {                                      // each page's four copies from its lane
+                const int z = page * 16;
+                tma_load_3d(Ks + lane * 2048, &tmk, 0, h, z, &bars->kv_full[stage]);
+                tma_load_3d(Ks + kPanel + lane * 2048, &tmk, 64, h, z, &bars->kv_full[stage]);
+                tma_load_3d(Vs + lane * 2048, &tmv, 0, h, z, &bars->kv_full[stage]);
+                tma_load_3d(Vs + kPanel + lane * 2048, &tmv, 64, h, z, &bars->kv_full[stage]);
             }
             __syncwarp();
         }
