@@ -167,7 +167,7 @@ def run_gpu(args):
              par=t(x.tree_parents), lg=t(x.target_logits), tok=t(x.draft_tokens),
              qp=None if w.greedy else t(x.draft_probs), u=None if w.greedy else t(x.uniforms))
     out = torch.empty_like(d["q"])
-    prob = ts.attn_problem(d["q"], d["k"], d["pt"])
+    prob = ts.attn_problem(d["q"], d["k"], d["pt"], kernel=args.attn_kernel)
     plan = ts.attn_plan(prob)
     ws_a = torch.empty(ts.attn_workspace_bytes(prob), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(ts.accept_workspace_bytes(w.batch, w.num_nodes, w.vocab), dtype=torch.uint8, device=dev)
@@ -178,9 +178,10 @@ def run_gpu(args):
 
     def step(inp):
         ts.tree_attn_verify(inp["q"], d["k"], d["v"], inp["pt"], inp["pl"], inp["par"], out,
-                            workspace=ws_a, stream=stream)
+                            kernel=args.attn_kernel, workspace=ws_a, stream=stream)
         ts.tree_accept(inp["lg"], inp["tok"], inp["qp"], inp["par"], inp["u"], w.temperature,
-                       accept_path=path, accept_len=alen, bonus_token=bonus, workspace=ws_b, stream=stream)
+                       accept_path=path, accept_len=alen, bonus_token=bonus, mode=args.accept_mode,
+                       workspace=ws_b, stream=stream)
 
     resident = dict(q=d["q"], pt=d["pt"], pl=d["pl"], par=d["par"], lg=d["lg"], tok=d["tok"], qp=d["qp"],
                     u=d["u"])
@@ -205,11 +206,11 @@ def run_gpu(args):
     for i in range(K):
         ev[i][0].record(stream)
         ts.tree_attn_verify(resident["q"], d["k"], d["v"], resident["pt"], resident["pl"], resident["par"], out,
-                            workspace=ws_a, stream=stream)
+                            kernel=args.attn_kernel, workspace=ws_a, stream=stream)
         ev[i][1].record(stream)
         ts.tree_accept(resident["lg"], resident["tok"], resident["qp"], resident["par"], resident["u"],
-                       w.temperature, accept_path=path, accept_len=alen, bonus_token=bonus, workspace=ws_b,
-                       stream=stream)
+                       w.temperature, accept_path=path, accept_len=alen, bonus_token=bonus, mode=args.accept_mode,
+                       workspace=ws_b, stream=stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     launches = ts.launch_count() - n0
@@ -297,6 +298,7 @@ def run_gpu(args):
         "t_attn_ms": round(t_attn, 4), "t_accept_ms": round(ms_step - t_attn, 4),
         "attn_plan": {"kernel": kernel_name, "num_splits": plan.num_splits, "split_tokens": plan.split_tokens,
                       "merge": bool(plan.merge)},
+        "accept_mode": ["auto", "all rows", "path only"][args.accept_mode],
         "mean_accept_len": round(float(lens.mean()), 3), "tokens_per_step": round(float(lens.mean()) + 1, 3),
         "roofline": roof,
         "e2e": {"value": round(world / (e2e_ms * 1e-3), 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
@@ -392,6 +394,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS) +
                     [f"{n}@b{b}" for n in gen.WORKLOADS for b in (1, 2, 8, 16, 32, 64)])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--attn-kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--accept-mode", type=int, default=0, help="0 auto, 1 all rows, 2 path only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()

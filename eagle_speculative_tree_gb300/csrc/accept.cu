@@ -26,6 +26,8 @@
 // Row passes use float4 loads when the vocabulary is a multiple of 4, compensated
 // float sums per thread and float64 across threads; the bonus draw scans one row with
 // float terms and float64 running sums.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace treespec {
@@ -579,6 +581,317 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
     }
 }
 
+// ------------------------------------------------------------ path-only, one cluster per sequence
+//
+// The same walk as accept_path_kernel, for large vocabularies: a cluster of CL CTAs
+// holds the current row in registers (thread t of CTA k owns tokens
+// [k*NT*E + t*E, +E)), so a residual pass is a few register operations per token
+// plus one cluster-wide reduction through distributed shared memory.  Every CTA takes
+// the same decisions from the same reduced scalars; CTA 0 writes the walk.
+
+namespace cg = cooperative_groups;
+
+template <int CL>
+struct ClusterRed {
+    float f[2][CL];
+    double d[2][CL];
+    int i[2][CL];
+};
+
+// Cluster-wide reductions: each CTA publishes one value, every CTA combines all CL
+// values in rank order (identical result everywhere).  Two alternating slots let a
+// slot be rewritten only after the next cluster barrier.
+template <int NT, int CL>
+struct ClusterReducer {
+    ClusterRed<CL>* cr;
+    double* redd;
+    float* redf;
+    int* redi;
+    int phase = 0;
+
+    __device__ double sum(double v) {
+        cg::cluster_group cl = cg::this_cluster();
+        v = block_sum_d<NT>(v, redd);
+        if (threadIdx.x == 0) cr->d[phase][cl.block_rank()] = v;
+        cl.sync();
+        double t = 0.0;
+        for (int k = 0; k < CL; ++k) t += cl.map_shared_rank(cr, k)->d[phase][k];
+        phase ^= 1;
+        return t;
+    }
+    __device__ float max(float v) {
+        cg::cluster_group cl = cg::this_cluster();
+        v = block_max_f<NT>(v, redf);
+        if (threadIdx.x == 0) cr->f[phase][cl.block_rank()] = v;
+        cl.sync();
+        float t = -INFINITY;
+        for (int k = 0; k < CL; ++k) t = fmaxf(t, cl.map_shared_rank(cr, k)->f[phase][k]);
+        phase ^= 1;
+        return t;
+    }
+    // (value, index): the largest value, lowest index on ties
+    __device__ int argmax(float best, int bi) {
+        cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+        }
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        __syncthreads();
+        if (lane == 0) { redf[warp] = best; redi[warp] = bi; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < NT / 32; ++w)
+                if (redf[w] > best || (redf[w] == best && redi[w] < bi)) { best = redf[w]; bi = redi[w]; }
+            cr->f[phase][cl.block_rank()] = best;
+            cr->i[phase][cl.block_rank()] = bi;
+        }
+        cl.sync();
+        float gb = -INFINITY;
+        int gi = 0x7fffffff;
+        for (int k = 0; k < CL; ++k) {
+            const ClusterRed<CL>* r = cl.map_shared_rank(cr, k);
+            const float vb = r->f[phase][k];
+            const int vi = r->i[phase][k];
+            if (vb > gb || (vb == gb && vi < gi)) { gb = vb; gi = vi; }
+        }
+        phase ^= 1;
+        return gi == 0x7fffffff ? 0 : gi;
+    }
+    // exclusive prefix (in rank order) of one double per CTA, and the total
+    __device__ double exclusive(double v, double* total) {
+        cg::cluster_group cl = cg::this_cluster();
+        if (threadIdx.x == 0) cr->d[phase][cl.block_rank()] = v;
+        cl.sync();
+        double pre = 0.0, t = 0.0;
+        for (int k = 0; k < CL; ++k) {
+            const double x = cl.map_shared_rank(cr, k)->d[phase][k];
+            if (k < int(cl.block_rank())) pre += x;
+            t += x;
+        }
+        phase ^= 1;
+        *total = t;
+        return pre;
+    }
+};
+
+template <int NT>
+__device__ __forceinline__ double block_exclusive_d(double v, double* scratch) {
+    // scratch: NT/32 + 1 doubles
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    double inc = warp_inclusive_scan_d(v);
+    __syncthreads();
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const double x = lane < NT / 32 ? scratch[lane] : 0.0;
+        const double wi = warp_inclusive_scan_d(x);
+        if (lane < NT / 32) scratch[lane] = wi - x;           // exclusive per warp
+    }
+    __syncthreads();
+    return scratch[warp] + (inc - v);
+}
+
+template <int CL, int NT, int E, bool STOCH>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_cluster_kernel(AcceptParams p) {
+    __shared__ int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
+    __shared__ float izs[kMaxNodes];
+    __shared__ double redd[32], scan[NT / 32 + 1];
+    __shared__ float redf[32];
+    __shared__ int redi[32];
+    __shared__ int s_cur, s_len, s_action, s_child, s_found;
+    __shared__ ClusterRed<CL> cred;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = int(cluster.block_rank());
+    const int b = blockIdx.y, tid = threadIdx.x;
+    const int N = p.N, V = p.V;
+    const int v0 = (rank * NT + tid) * E;                    // first token of this thread
+    ClusterReducer<NT, CL> red{&cred, redd, redf, redi, 0};
+
+    for (int c = tid; c < N; c += NT) {
+        par[c] = p.parents[size_t(b) * N + c];
+        tok[c] = p.tokens[size_t(b) * N + c];
+    }
+    if (tid == 0) {
+        s_cur = 0;
+        s_len = 0;
+    }
+    __syncthreads();
+    uint32_t st = (tid == 0 && rank == 0) ? check_parents(par, N) : 0u;
+
+    float r[E], qv[E];
+    int amax = 0, rej = 0;
+    float M2 = 0.f, invS = 1.f;
+    for (int depth = 0; depth < N; ++depth) {
+        const int cur = s_cur;
+        const size_t row = size_t(b) * N + cur;
+        const float* lg = p.logits + row * V;
+        const float* qr = STOCH ? p.probs + row * V : nullptr;
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+            const int v = v0 + e;
+            float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (v < V) {
+                x = __ldg(reinterpret_cast<const float4*>(lg + v));
+                if (STOCH) y = __ldg(reinterpret_cast<const float4*>(qr + v));
+            }
+            r[e] = x.x; r[e + 1] = x.y; r[e + 2] = x.z; r[e + 3] = x.w;
+            qv[e] = y.x; qv[e + 1] = y.y; qv[e + 2] = y.z; qv[e + 3] = y.w;
+        }
+        if constexpr (!STOCH) {
+            float best = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (r[e] > best) { best = r[e]; bi = v0 + e; }
+            amax = red.argmax(best, bi);
+        } else {
+            float m = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < E; ++e) m = fmaxf(m, r[e]);
+            M2 = red.max(m) * p.c;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                r[e] = ex2(fmaf(r[e], p.c, -M2));                 // -inf (padding) -> 0
+                ls[e & 3] += r[e];
+            }
+            invS = 1.f / float(red.sum((double(ls[0]) + double(ls[1])) + (double(ls[2]) + double(ls[3]))));
+#pragma unroll
+            for (int e = 0; e < E; ++e) r[e] *= invS;               // r = p, as prob_at
+        }
+        int jj = 0, pos = cur, action = 0, child = -1;
+        for (;;) {
+            if (tid == 0) {
+                int nc = -1;
+                for (int k = pos + 1; k < N; ++k)
+                    if (par[k] == cur) { nc = k; break; }
+                int act = 0;
+                if (nc >= 0) {
+                    const int x = tok[nc];
+                    const bool valid = x >= 0 && x < V;
+                    if (!valid && rank == 0) st |= TREESPEC_STATUS_BAD_TOKEN;
+                    bool ok = false;
+                    if (valid) {
+                        if (!STOCH) {
+                            ok = x == amax;
+                        } else {
+                            const float qx = __ldg(qr + x);
+                            const float rx = residual_at(prob_at(__ldg(lg + x), p.c, M2, invS), qx, izs, jj);
+                            ok = rx > 0.f && p.uniforms[size_t(b) * N + nc] * qx <= rx;
+                        }
+                    }
+                    if (ok) {
+                        act = 1;
+                    } else {
+                        int more = -1;
+                        for (int k = nc + 1; k < N; ++k)
+                            if (par[k] == cur) { more = k; break; }
+                        act = more >= 0 ? 2 : 3;
+                    }
+                }
+                s_action = act;
+                s_child = nc;
+            }
+            __syncthreads();
+            action = s_action;
+            child = s_child;
+            __syncthreads();
+            if (action == 1 || action == 0) break;
+            ++jj;
+            if (action == 3) break;
+            if constexpr (STOCH) {                          // the next sibling sees the residual
+                float zs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < E; ++e) zs4[e & 3] += fmaxf(r[e] - qv[e], 0.f);
+                const double Z = red.sum((double(zs4[0]) + double(zs4[1])) + (double(zs4[2]) + double(zs4[3])));
+                const float iz = float(Z) > 0.f ? 1.f / float(Z) : 0.f;
+                if (tid == 0) izs[jj - 1] = iz;
+                if (iz > 0.f) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) r[e] = fmaxf(r[e] - qv[e], 0.f) * iz;
+                }
+                __syncthreads();
+            }
+            pos = child;
+        }
+        if (action != 1) {
+            rej = jj;
+            break;
+        }
+        if (tid == 0) {
+            path[s_len] = child;
+            s_len = s_len + 1;
+            s_cur = child;
+        }
+        __syncthreads();
+    }
+    const int len = s_len;
+    if (rank == 0) {
+        if (tid == 0 && st) atomicOr(p.status, st);
+        for (int c = tid; c < N; c += NT) p.path[size_t(b) * N + c] = c < len ? path[c] : -1;
+        if (tid == 0) p.len[b] = len;
+        if (!STOCH && tid == 0) p.bonus[b] = amax;
+    }
+    if constexpr (STOCH) {
+        // bonus token: inverse CDF of r_rej (up to normalisation) in token order
+        float w[E];
+        bool unchanged = false;
+        double total = 0.0, mine = 0.0;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            mine = 0.0;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                w[e] = (rej == 0 || unchanged) ? r[e] : fmaxf(r[e] - qv[e], 0.f);
+                mine += double(w[e]);
+            }
+            total = red.sum(mine);
+            if (total > 0.0 || rej == 0 || unchanged) break;
+            unchanged = true;                                // zero residual mass: keep r_{rej-1}
+        }
+        double cta_total = 0.0;
+        const double pre_thread = block_exclusive_d<NT>(mine, scan);
+        // total of this CTA = last thread's exclusive prefix + its own share
+        if (tid == NT - 1) scan[NT / 32] = pre_thread + mine;
+        __syncthreads();
+        cta_total = scan[NT / 32];
+        double all = 0.0;
+        const double pre_cta = red.exclusive(cta_total, &all);
+        const double thr = double(p.uniforms[size_t(b) * N]) * total;
+        const double base = pre_cta + pre_thread;
+        if (tid == 0 && rank == 0) s_found = 0;
+        cluster.sync();
+        if (base <= thr && thr < base + mine) {              // the crossing lies in this thread's tokens
+            double run = base;
+            int v = -1, last_nz = -1;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                if (w[e] > 0.f) last_nz = v0 + e;
+                run += double(w[e]);
+                if (v < 0 && run > thr) v = v0 + e;
+            }
+            p.bonus[b] = v >= 0 ? v : last_nz;
+            *cluster.map_shared_rank(&s_found, 0) = 1;
+        }
+        cluster.sync();
+        if (rank == 0 && tid == 0 && s_found == 0) s_found = 2;     // nobody: rounding at the top end
+        cluster.sync();
+        const int none = *cluster.map_shared_rank(&s_found, 0) == 2;
+        if (none) {
+            int last_nz = -1;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (w[e] > 0.f) last_nz = v0 + e;
+            const int ln = red.argmax(float(last_nz), last_nz);  // largest index with mass
+            if (rank == 0 && tid == 0) p.bonus[b] = ln < 0 ? 0 : ln;
+        }
+    }
+    cluster.sync();                      // peers may still read this CTA's shared memory
+}
+
 // ------------------------------------------------------------ launches
 
 template <int NT, bool STOCH>
@@ -597,6 +910,19 @@ void path_launch(const AcceptParams& p, cudaStream_t s) {
 template <bool STOCH>
 int launch_schedule(const AcceptParams& p, int mode, cudaStream_t s) {
     if (mode == TREESPEC_ACCEPT_PATH_ONLY) {
+        const bool vec = p.V % 4 == 0 && p.B <= 65535;
+        if (vec && p.V > 16384 && p.V <= 32768) {
+            accept_cluster_kernel<2, 512, 32, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
+            return 1;
+        }
+        if (vec && p.V > 32768 && p.V <= 65536) {
+            accept_cluster_kernel<4, 512, 32, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
+            return 1;
+        }
+        if (vec && p.V > 65536 && p.V <= 131072) {
+            accept_cluster_kernel<8, 512, 32, STOCH><<<dim3(8, p.B), 512, 0, s>>>(p);
+            return 1;
+        }
         if (p.V >= 32768) path_launch<512, STOCH>(p, s);
         else if (p.V >= 1024) path_launch<256, STOCH>(p, s);
         else path_launch<32, STOCH>(p, s);

@@ -50,13 +50,13 @@ enum treespec_dtype {
 };
 
 enum treespec_kernel {
-    TREESPEC_KERNEL_AUTO = 0,  /* tensor-core kernel when N*G >= 64 rows and bf16, else CUDA cores */
+    TREESPEC_KERNEL_AUTO = 0,  /* tensor-core kernel for bf16 with head_dim 128, else CUDA cores */
     TREESPEC_KERNEL_SIMT = 1,  /* CUDA-core split-KV kernel (any dtype) */
     TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128) */
 };
 
 enum treespec_accept_mode {
-    TREESPEC_ACCEPT_AUTO = 0,       /* path-only when B*N*V is large, all rows otherwise */
+    TREESPEC_ACCEPT_AUTO = 0,       /* path-only */
     TREESPEC_ACCEPT_ALL_ROWS = 1,   /* reduce every (sequence, node) row, then walk */
     TREESPEC_ACCEPT_PATH_ONLY = 2,  /* walk first; reduce only the rows the walk visits */
 };

@@ -50,8 +50,8 @@ def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
     assert_attention_close(out, oracle_attention(x), w.dtype)
 
 
-def test_auto_plan_picks_tensor_cores_from_64_rows(ts, cuda_device):
-    for name, want in [("c2_llama3_8b_bf16_greedy", 1), ("c3_llama2_7b_bf16_stoch", 1),
+def test_auto_plan_picks_tensor_cores_for_bf16_head128(ts, cuda_device):
+    for name, want in [("c2_llama3_8b_bf16_greedy", 2), ("c3_llama2_7b_bf16_stoch", 2),
                        ("c4_llama3_70b_bf16_greedy", 2), ("c5_ragged_b64_bf16_stoch", 2),
                        ("c1_tiny_f32_greedy", 1)]:
         w = gen.get(name)
