@@ -65,6 +65,10 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// CL > 1: the CL CTAs of a cluster hold consecutive row blocks of the same
+// (sequence, kv head, split); each issues the TMA copies of every CL-th page of a tile
+// multicast to all of them, and a stage is refilled only after all CL CTAs released it.
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
             mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->kv_empty[s], CL);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
@@ -126,6 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (CL > 1) cluster_sync_all();      // peers' barriers exist before any multicast
+    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+    constexpr uint16_t kMask = uint16_t((1u << CL) - 1u);
     const uint32_t tbase = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
 
@@ -195,14 +202,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
             if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[stage], uint32_t(__popc(viatma)) * 4u * 2048u);
             __syncwarp();
-            if (kind == 1) {                                      // each page's four copies from its lane
+            if (kind == 1 && (CL == 1 || (lane % CL) == int(rank))) {   // each page's four copies
                 const int z = page * 16;
-                tma_load_3d(Ks + lane * 2048, &tmk, 0, h, z, &bars->kv_full[stage]);
-                tma_load_3d(Ks + kPanel + lane * 2048, &tmk, 64, h, z, &bars->kv_full[stage]);
-                tma_load_3d(Vs + lane * 2048, &tmv, 0, h, z, &bars->kv_full[stage]);
-                tma_load_3d(Vs + kPanel + lane * 2048, &tmv, 64, h, z, &bars->kv_full[stage]);
+                if constexpr (CL == 1) {
+                    tma_load_3d(Ks + lane * 2048, &tmk, 0, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(Ks + kPanel + lane * 2048, &tmk, 64, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(Vs + lane * 2048, &tmv, 0, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(Vs + kPanel + lane * 2048, &tmv, 64, h, z, &bars->kv_full[stage]);
+                } else {
+                    tma_load_3d_multicast(Ks + lane * 2048, &tmk, 0, h, z, &bars->kv_full[stage], kMask);
+                    tma_load_3d_multicast(Ks + kPanel + lane * 2048, &tmk, 64, h, z, &bars->kv_full[stage], kMask);
+                    tma_load_3d_multicast(Vs + lane * 2048, &tmv, 0, h, z, &bars->kv_full[stage], kMask);
+                    tma_load_3d_multicast(Vs + kPanel + lane * 2048, &tmv, 64, h, z, &bars->kv_full[stage], kMask);
+                }
             }
             __syncwarp();
+        }
+        if constexpr (CL > 1) {
+            // every peer's release of every stage has landed here before this CTA may exit
+            for (int s2 = 0; s2 < kNS && s2 < ntiles; ++s2) {
+                const int uses = (ntiles - s2 + kNS - 1) / kNS;
+                if (!mbar_wait_bounded(&bars->kv_empty[s2], (uses - 1) & 1, kWaitNs)) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+                }
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -238,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ts(tbase + kColO, pcol + kk * 8, smem_desc(vaddr + kk * 2048, kPanel, 1024), kIdO,
                                 (j > 0 || kk > 0));
                 }
-                mma_commit(&bars->kv_empty[stage]);
+                if constexpr (CL == 1) mma_commit(&bars->kv_empty[stage]);
+                else mma_commit_multicast(&bars->kv_empty[stage], kMask);
                 mma_commit(&bars->p_free[j & 1]);
                 return true;
             };
@@ -430,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+    if constexpr (CL > 1) cluster_sync_all();      // no peer still writes into this CTA
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -465,16 +491,40 @@ bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_t
 
 bool attn_tc_supported(int dtype, int D) { return dtype == TREESPEC_DTYPE_BF16 && D == kD; }
 
+template <int CL>
+cudaError_t launch_cluster(const AttnParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s) {
+    auto kern = attn_tc_kernel<CL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_splits, p.Hkv * p.row_blocks, p.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = CL;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+int attn_tc_cluster_size(int row_blocks) { return row_blocks % 4 == 0 ? 4 : row_blocks % 2 == 0 ? 2 : 1; }
+
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
     CUtensorMap mk, mv;
     const long long pool_tokens = (long long)p.num_pool_pages * p.ps;
     if (!make_pool_map(&mk, p.k, p.Hkv, pool_tokens) || !make_pool_map(&mv, p.v, p.Hkv, pool_tokens))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    dim3 grid(p.num_splits, p.Hkv * p.row_blocks, p.B);
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, mk, mv);
-    return cudaGetLastError();
+    switch (attn_tc_cluster_size(p.row_blocks)) {
+        case 4: return launch_cluster<4>(p, mk, mv, s);
+        case 2: return launch_cluster<2>(p, mk, mv, s);
+        default: return launch_cluster<1>(p, mk, mv, s);
+    }
 }
 
 }  // namespace treespec

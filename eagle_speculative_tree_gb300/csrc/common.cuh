@@ -103,6 +103,7 @@ cudaError_t launch_tree_prologue(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
 bool attn_tc_supported(int dtype, int D);
+int attn_tc_cluster_size(int row_blocks);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptParams& p, int mode, cudaStream_t s, int* kernels);
 size_t attn_simt_smem_bytes(int dtype, int D, int R_block);

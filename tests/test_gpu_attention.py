@@ -82,7 +82,7 @@ def _custom(name, parents, prefix, batch=None):
 @pytest.mark.parametrize("dtype_cfg,kernel", [("c1_tiny_f32_greedy", 1), ("c2_llama3_8b_bf16_greedy", 1),
                                               ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2)])
 @pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
-                                  "random64"])
+                                  "random64", "random32"])
 def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
     rng = np.random.default_rng(hash(case) % 2**32)
     if case == "single_node":
@@ -95,6 +95,8 @@ def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
         parents, prefix = [trees.chain(64)], [129]
     elif case == "star64":
         parents, prefix = [trees.star(64)], [40]
+    elif case == "random32":
+        parents, prefix = [trees.random_recursive(rng, 32), trees.random_recursive(rng, 32)], [700, 3]
     else:
         parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
     w, x = _custom(dtype_cfg, parents, prefix)
