@@ -12,8 +12,8 @@
 //   * warp 1 allocates all 512 TMEM columns (S and P double-buffered, O) and issues
 //     S = Q K^T from shared memory and O += P V with P read from TMEM, as
 //     128x128x16 tcgen05.mma instructions;
-//   * warps 2-5 (one TMEM lane quarter each, one query row per thread) read S from
-//     TMEM, apply the tree mask -- prefix tokens always, tree token S+j only when bit
+//   * warps 2-9 (two per TMEM lane quarter, one query row per thread, each warp one
+//     half of the tile's columns) read S from TMEM, apply the tree mask -- prefix tokens always, tree token S+j only when bit
 //     j of the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2
 //     mask M and section 5 bitmask) -- run the online softmax in base 2, write P as
 //     packed bf16 back to TMEM, and rescale O in TMEM only when a row's running max
@@ -38,7 +38,7 @@ constexpr int kBN = 128;             // tokens per tile
 constexpr int kNS = 3;               // K/V ring stages
 constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
 constexpr int kTile = 2 * kPanel;    // [128][128] bf16
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;           // producer, MMA, 8 softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;        // S double buffer: columns [0, 256)
 constexpr uint32_t kColP = 256;      // P double buffer (bf16 pairs): [256, 384)
@@ -52,8 +52,11 @@ constexpr int kOffV = kOffK + kNS * kTile;
 constexpr int kOffBar = kOffV + kNS * kTile;
 constexpr int kNumBars = 2 * kNS + 2 + 2 + 2 + 2 + 2;   // kv_full/empty, s_full/empty, p_full, p_free, q_full, drain
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffAnc = (kOffMisc + 16 + 7) / 8 * 8;
-constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8 + 1024;   // + alignment slack
+constexpr int kOffFlag = kOffMisc + 16;                     // exchange sequence numbers, 4 quarters x 2 halves
+constexpr int kOffXch = kOffFlag + 32;                      // softmax half-row exchange, 2 x 2 x 128 floats
+constexpr int kOffAnc = kOffXch + 2 * 2 * 128 * 4;
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 232,112 bytes: within the 227 KB limit
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
     uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], s_empty[2], p_full[2], p_free[2], q_full, drain;
@@ -72,9 +75,9 @@ template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // the swizzled tiles need 1024-byte alignment: the dynamic shared memory of this
+    // kernel (which has no static shared memory) starts at the window's base
+    extern __shared__ __align__(1024) unsigned char sm[];
     Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
@@ -105,6 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t1 = min(L, t0 + p.split_tokens);
     if (t0 >= t1) return;
     const int ntiles = (t1 - t0 + kBN - 1) / kBN;
+    if (smem_u32(sm) & 1023u) {                    // never expected; refuse rather than misread tiles
+        if (tid == 0) atomicOr(p.status, TREESPEC_STATUS_INTERNAL);
+        return;
+    }
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -113,13 +120,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->s_empty[s], 128);
-            mbar_init(&bars->p_full[s], 128);
+            mbar_init(&bars->s_empty[s], 256);
+            mbar_init(&bars->p_full[s], 256);
             mbar_init(&bars->p_free[s], 1);
         }
-        mbar_init(&bars->q_full, 128);
+        mbar_init(&bars->q_full, 256);
         mbar_init(&bars->drain, 1);
         *abort_flag = 0;
+        for (int f = 0; f < 8; ++f) reinterpret_cast<volatile int*>(sm + kOffFlag)[f] = 0;
         fence_mbar_init();
     }
     for (int e = tid; e < p.N; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N + e];
@@ -282,8 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax warpgroup
+        // ------------------------------------------------------------ softmax warps
+        // Eight warps: warp w owns TMEM lane quarter (w % 4) = 32 query rows, and one
+        // half of the tile's columns (warps 2-5: columns 0-63, warps 6-9: 64-127).  The
+        // two warps of a quarter swap their half-row maxima through shared memory.
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;                    // 0 or 1
         const int t = quarter * 32 + lane;                   // query row in the block = TMEM lane
         const int r = r0 + t;
         const bool row_ok = r < p.R;
@@ -292,34 +304,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t anc = row_ok ? anc_s[i] : 0ull;
         const bool warp_rows = __any_sync(0xffffffffu, row_ok);
         const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
+        volatile float* xch = reinterpret_cast<volatile float*>(sm + kOffXch);  // [2 parity][2 half][128 rows]
+        volatile int* flags = reinterpret_cast<volatile int*>(sm + kOffFlag);   // [4 quarter][2 half]
+        // Swap one float per row with the other half's warp of this quarter: publish the
+        // value, then the sequence number; wait (bounded) for the partner's number.  Two
+        // parity slots: slot seq&1 is rewritten only after the partner has moved past seq.
+        auto exchange = [&](float value, int seq, bool* ok) -> float {
+            xch[((seq & 1) * 2 + half) * 128 + t] = value;
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) flags[quarter * 2 + half] = seq;
+            bool good = true;
+            if (lane == 0 && flags[quarter * 2 + (half ^ 1)] < seq) {
+                const uint64_t t_start = global_ns();
+                while (flags[quarter * 2 + (half ^ 1)] < seq) {
+                    if (global_ns() - t_start > kWaitNs) { good = false; break; }
+                }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            __threadfence_block();
+            *ok = good;
+            return xch[((seq & 1) * 2 + (half ^ 1)) * 128 + t];
+        };
         {
             const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                               ((size_t(b) * p.N + i) * p.Hq + hq) * kD);
+                                                               ((size_t(b) * p.N + i) * p.Hq + hq) * kD) + half * 8;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 const uint4 v = row_ok ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + kOffQ + (c >> 3) * kPanel + sw128_offset(t, c & 7)) = v;
+                *reinterpret_cast<uint4*>(sm + kOffQ + half * kPanel + sw128_offset(t, c)) = v;
             }
         }
         fence_proxy_async_smem();
         mbar_arrive(&bars->q_full);
 
         const float sc = p.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
+        float m_used = -INFINITY, l = 0.f;                   // l: this warp's half of the row sum
         bool alive = true;
         for (int j = 0; j < ntiles && alive; ++j) {
             const int base = t0 + j * kBN;
             if (!mbar_wait_bounded(&bars->s_full[j & 1], (j >> 1) & 1, kWaitNs)) { alive = false; break; }
             tc_fence_after();
-            // which of the tile's 128 columns this row may see, as four 32-bit words:
-            // prefix columns below pref_end, tree columns [tree_lo, tree_hi) through the
-            // node's ancestor word
+            // which of this half's 64 columns the row may see, as two 32-bit words: prefix
+            // columns below pref_end, tree columns [tree_lo, tree_hi) via the ancestor word
             const int pref_end = min(S, t1) - base;
             const int tree_lo = S - base, tree_hi = t1 - base;
-            uint32_t mw[4];
+            uint32_t mw[2];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int lo = 32 * w;
+            for (int w = 0; w < 2; ++w) {
+                const int lo = 64 * half + 32 * w;
                 const int np = min(max(pref_end - lo, 0), 32);
                 uint32_t bits = np == 32 ? 0xffffffffu : ((1u << np) - 1u);
                 const int nh = min(max(tree_hi - lo, 0), 32);
@@ -331,12 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bits |= tb & hi_mask;
                 mw[w] = row_ok ? bits : 0u;
             }
-            const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu);
-            // raw scores of the whole row in one TMEM round trip, masked in place
-            uint32_t v[kBN];
+            const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
+            uint32_t v[kBN / 2];
             if (warp_rows) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tl + kColS + uint32_t(j & 1) * 128u + c * 32, v + c * 32);
+                tmem_ld32(tl + kColS + uint32_t(j & 1) * 128u + half * 64, v);
+                tmem_ld32(tl + kColS + uint32_t(j & 1) * 128u + half * 64 + 32, v + 32);
                 tmem_wait_ld();
             }
             tc_fence_before();
@@ -344,12 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kNegInf = 0xff800000u;
             if (!full) {
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
+                for (int c = 0; c < kBN / 2; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
-            const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            for (int c = 0; c < kBN / 2; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+            float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            // the row's max over both halves (identical in the two warps of the quarter)
+            bool xok = true;
+            mraw = fmaxf(mraw, exchange(mraw, j + 1, &xok));
+            if (!xok) { alive = false; break; }
             const float mt = mraw * sc;                    // scale > 0 commutes with max
             bool resc = false;
             float alpha = 1.f;
@@ -360,26 +396,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = mt;
             }
             const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-            // probabilities 2^(s*scale - m), rounded to bf16 and packed in pairs
-            // (packed in place: pair c lands in v[c], after v[2c] and v[2c+1] were read)
+            // probabilities 2^(s*scale - m), rounded to bf16 and packed in pairs in place
             uint32_t* pk = v;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < kBN / 2; ++c) {
+            for (int c = 0; c < kBN / 4; ++c) {
                 const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, -msub));
                 const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, -msub));
                 pk[c] = pack_bf16x2(p0, p1);
                 ls[c & 3] += p0 + p1;
             }
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            l += lsum;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // P buffer j&1 is free once P_{j-2} V_{j-2} has completed
             if (j >= 2 && !mbar_wait_bounded(&bars->p_free[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) {
                 alive = false;
                 break;
             }
             if (__any_sync(0xffffffffu, resc)) {
-                // O may only be rescaled once P_{j-1} V_{j-1} is in it
+                // O may only be rescaled once P_{j-1} V_{j-1} is in it (this warp's 64 columns)
                 if (!mbar_wait_bounded(&bars->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitNs)) {
                     alive = false;
                     break;
@@ -387,20 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float f = resc ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tl + kColO + c * 32, o);
+                    tmem_ld32(tl + kColO + half * 64 + c * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st32(tl + kColO + c * 32, o);
+                    tmem_st32(tl + kColO + half * 64 + c * 32, o);
                 }
             }
             tc_fence_after();
-            if (warp_rows) {
-                tmem_st32(tl + kColP + uint32_t(j & 1) * 64u, pk);
-                tmem_st32(tl + kColP + uint32_t(j & 1) * 64u + 32u, pk + 32);
-            }
+            if (warp_rows) tmem_st32(tl + kColP + uint32_t(j & 1) * 64u + half * 32, pk);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full[j & 1]);
@@ -410,18 +441,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
         } else if (mbar_wait_bounded(&bars->p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, kWaitNs)) {
             tc_fence_after();
-            const float inv = 1.f / l;
+            // the row sum over both halves
+            bool xok = true;
+            const float lrow = l + exchange(l, ntiles + 1, &xok);
+            if (!xok) {
+                *abort_flag = 1;
+                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+            }
+            const float inv = 1.f / lrow;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t o[32];
                 if (warp_rows) {
-                    tmem_ld32(tl + kColO + c * 32, o);
+                    tmem_ld32(tl + kColO + half * 64 + c * 32, o);
                     tmem_wait_ld();
                 }
                 if (!row_ok) continue;
+                const int col0 = half * 64 + c * 32;
                 if (!p.merge) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                          ((size_t(b) * p.N + i) * p.Hq + hq) * kD + c * 32);
+                                                          ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         uint32_t w4[4];
@@ -434,14 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     const size_t pr = (size_t(b * p.Hkv + h) * p.num_splits + split) * p.R + r;
-                    float4* dst = reinterpret_cast<float4*>(p.part_acc + pr * kD + c * 32);
+                    float4* dst = reinterpret_cast<float4*>(p.part_acc + pr * kD + col0);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
                                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-                    if (c == 0) {
+                    if (c == 0 && half == 0) {
                         p.part_ml[pr * 2] = m_used;
-                        p.part_ml[pr * 2 + 1] = l;
+                        p.part_ml[pr * 2 + 1] = lrow;
                     }
                 }
             }

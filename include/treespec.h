@@ -79,6 +79,7 @@ enum treespec_status_bits {
     TREESPEC_STATUS_BAD_LENGTH = 1u << 2,  /* prefix_len < 0 or prefix_len + N > pages * page_size */
     TREESPEC_STATUS_BAD_TOKEN = 1u << 3,   /* a draft token outside [0, vocab) */
     TREESPEC_STATUS_TIMEOUT = 1u << 4,     /* a bounded wait inside a kernel ran out */
+    TREESPEC_STATUS_INTERNAL = 1u << 5,    /* a launch-configuration invariant failed (work skipped) */
 };
 
 /* ------------------------------------------------------------------ tree attention */
