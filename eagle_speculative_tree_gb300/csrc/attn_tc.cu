@@ -4,11 +4,11 @@
 // computed with tcgen05:
 //   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
 //     are zero) x one split of the sequence's logical tokens, in 128-token tiles;
-//   * warp 0 streams the split's K and V pages with TMA (one 16-token page x 64
-//     head-dim columns per copy, 128-byte swizzle; lanes 0-7 issue one page each)
-//     into a three-stage ring; the partly filled last page of a sequence and pages
-//     past the split are written by the warp itself, zero-filled, so nothing outside
-//     the sequence reaches the MMA;
+//   * warp 0 streams the split's K pages and warp 10 its V pages with TMA (one
+//     16-token page x 64 head-dim columns per copy, 128-byte swizzle; lanes 0-7 issue
+//     one page each) into two three-stage rings; the partly filled last page of a
+//     sequence and pages past the split are written by the warp itself, zero-filled,
+//     so nothing outside the sequence reaches the MMA;
 //   * warp 1 allocates all 512 TMEM columns (S and P double-buffered, O) and issues
 //     S = Q K^T from shared memory and O += P V with P read from TMEM, as
 //     128x128x16 tcgen05.mma instructions;
@@ -38,7 +38,8 @@ constexpr int kBN = 128;             // tokens per tile
 constexpr int kNS = 3;               // K/V ring stages
 constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
 constexpr int kTile = 2 * kPanel;    // [128][128] bf16
-constexpr int kThreads = 320;           // producer, MMA, 8 softmax warps
+constexpr int kThreads = 352;        // K producer, MMA, 8 softmax warps, V producer
+constexpr int kWarpV = 10;           // the V producer warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;        // S double buffer: columns [0, 256)
 constexpr uint32_t kColP = 256;      // P double buffer (bf16 pairs): [256, 384)
@@ -50,16 +51,16 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;
 constexpr int kOffV = kOffK + kNS * kTile;
 constexpr int kOffBar = kOffV + kNS * kTile;
-constexpr int kNumBars = 2 * kNS + 2 + 2 + 2 + 2 + 2;   // kv_full/empty, s_full/empty, p_full, p_free, q_full, drain
+constexpr int kNumBars = 4 * kNS + 2 + 2 + 2 + 2 + 2;   // k/v full/empty, s_full/empty, p_full, p_free, q_full, drain
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffFlag = kOffMisc + 16;                     // exchange sequence numbers, 4 quarters x 2 halves
 constexpr int kOffXch = kOffFlag + 32;                      // softmax half-row exchange, 2 x 2 x 128 floats
 constexpr int kOffAnc = kOffXch + 2 * 2 * 128 * 4;
-constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 232,112 bytes: within the 227 KB limit
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 232,160 bytes: within the 227 KB limit
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t kv_full[kNS], kv_empty[kNS], s_full[2], s_empty[2], p_full[2], p_free[2], q_full, drain;
+    uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS], s_full[2], s_empty[2], p_full[2], p_free[2], q_full, drain;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -115,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(&bars->kv_full[s], 1);
-            mbar_init(&bars->kv_empty[s], CL);
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], CL);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], CL);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
@@ -144,13 +147,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == kWarpV) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 0 streams K, warp 10 streams V: a K stage is free again as soon as S of
+        // its tile has been computed, a V stage only after P V, so each has its own ring.
+        const bool is_v = warp == kWarpV;
+        uint64_t* full = is_v ? bars->v_full : bars->k_full;
+        uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+        const uint16_t* src = static_cast<const uint16_t*>(is_v ? p.v : p.k);
+        const CUtensorMap* map = is_v ? &tmv : &tmk;
+        unsigned char* ring = sm + (is_v ? kOffV : kOffK);
         const int* ptab = p.page_table + size_t(b) * p.max_pages;
-        if (lane == 0) {
-            tma_prefetch_desc(&tmk);
-            tma_prefetch_desc(&tmv);
-        }
+        if (lane == 0) tma_prefetch_desc(map);
         // page ids of tile j (lane k < 8 holds page k of the tile), fetched one tile ahead
         auto fetch_pages = [&](int j) -> int {
             const int pos0 = t0 + j * kBN + lane * 16;
@@ -161,11 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int stage = j % kNS;
             int page = page_next;
             page_next = fetch_pages(j + 1);
-            if (j >= kNS && !mbar_wait_bounded(&bars->kv_empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
-                *abort_flag = 1;
-                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-            }
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             const int base = t0 + j * kBN;
             // lanes 0..7 own page `lane` of the tile: 1 = full page by TMA, 2 = written here
             // (the sequence's partly filled last page, a bad page id, or past the split)
@@ -182,8 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     page = -1;
                 }
             }
-            unsigned char* Ks = sm + kOffK + stage * kTile;
-            unsigned char* Vs = sm + kOffV + stage * kTile;
+            if (j >= kNS && !mbar_wait_bounded(&empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+            }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            unsigned char* dst = ring + stage * kTile;
             const unsigned manual = __ballot_sync(0xffffffffu, kind == 2);
             if (manual) {
                 for (int pg = 0; pg < 8; ++pg) {
@@ -193,35 +200,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = lane; c < 16 * 16; c += 32) {      // 16 token rows x 16 chunks of 16 bytes
                         const int rr = c >> 4, ch = c & 15;
                         const int pos = q0 + rr;
-                        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+                        uint4 val = make_uint4(0, 0, 0, 0);
                         if (pgid >= 0 && pos < t1) {
                             const size_t off = ((size_t(pgid) * p.ps + (pos & 15)) * p.Hkv + h) * kD + ch * 8;
-                            kv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.k) + off));
-                            vv = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.v) + off));
+                            val = __ldg(reinterpret_cast<const uint4*>(src + off));
                         }
-                        const uint32_t o = (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7);
-                        *reinterpret_cast<uint4*>(Ks + o) = kv;
-                        *reinterpret_cast<uint4*>(Vs + o) = vv;
+                        *reinterpret_cast<uint4*>(dst + (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7)) = val;
                     }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
             const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
-            if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[stage], uint32_t(__popc(viatma)) * 4u * 2048u);
+            if (lane == 0) mbar_arrive_expect_tx(&full[stage], uint32_t(__popc(viatma)) * 2u * 2048u);
             __syncwarp();
-            if (kind == 1 && (CL == 1 || (lane % CL) == int(rank))) {   // each page's four copies
+            if (kind == 1 && (CL == 1 || (lane % CL) == int(rank))) {   // each page's two copies
                 const int z = page * 16;
                 if constexpr (CL == 1) {
-                    tma_load_3d(Ks + lane * 2048, &tmk, 0, h, z, &bars->kv_full[stage]);
-                    tma_load_3d(Ks + kPanel + lane * 2048, &tmk, 64, h, z, &bars->kv_full[stage]);
-                    tma_load_3d(Vs + lane * 2048, &tmv, 0, h, z, &bars->kv_full[stage]);
-                    tma_load_3d(Vs + kPanel + lane * 2048, &tmv, 64, h, z, &bars->kv_full[stage]);
+                    tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
+                    tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
                 } else {
-                    tma_load_3d_multicast(Ks + lane * 2048, &tmk, 0, h, z, &bars->kv_full[stage], kMask);
-                    tma_load_3d_multicast(Ks + kPanel + lane * 2048, &tmk, 64, h, z, &bars->kv_full[stage], kMask);
-                    tma_load_3d_multicast(Vs + lane * 2048, &tmv, 0, h, z, &bars->kv_full[stage], kMask);
-                    tma_load_3d_multicast(Vs + kPanel + lane * 2048, &tmv, 64, h, z, &bars->kv_full[stage], kMask);
+                    tma_load_3d_multicast(dst + lane * 2048, map, 0, h, z, &full[stage], kMask);
+                    tma_load_3d_multicast(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage], kMask);
                 }
             }
             __syncwarp();
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // every peer's release of every stage has landed here before this CTA may exit
             for (int s2 = 0; s2 < kNS && s2 < ntiles; ++s2) {
                 const int uses = (ntiles - s2 + kNS - 1) / kNS;
-                if (!mbar_wait_bounded(&bars->kv_empty[s2], (uses - 1) & 1, kWaitNs)) {
+                if (!mbar_wait_bounded(&empty[s2], (uses - 1) & 1, kWaitNs)) {
                     *abort_flag = 1;
                     atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
                 }
@@ -238,47 +238,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Order S_0, S_1, then S_{j+2} before P_j V_j: the next scores are already queued
+        // when the softmax hands over P_j, so the softmax warps never wait for S.
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
             constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
-            const uint32_t qaddr = sbase + kOffQ;
+            // descriptors of the first K-step of Q, of ring stage 0 of K and of V; a
+            // step or a stage moves only the start-address field (address >> 4 in the
+            // low 14 bits, which no offset inside the 227 KB window overflows)
+            const uint64_t dq = smem_desc(sbase + kOffQ, 16, 1024);
+            const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
+            const uint64_t dv = smem_desc(sbase + kOffV, kPanel, 1024);
             bool ok = mbar_wait_bounded(&bars->q_full, 0, kWaitNs);
             auto issue_s = [&](int j) -> bool {
                 const int stage = j % kNS;
-                if (!mbar_wait_bounded(&bars->kv_full[stage], (j / kNS) & 1, kWaitNs)) return false;
+                if (!mbar_wait_bounded(&bars->k_full[stage], (j / kNS) & 1, kWaitNs)) return false;
                 if (j >= 2 && !mbar_wait_bounded(&bars->s_empty[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) return false;
                 tc_fence_after();
-                const uint32_t kaddr = sbase + kOffK + stage * kTile;
+                const uint64_t kb = dk + uint64_t((stage * kTile) >> 4);
                 const uint32_t d = tbase + kColS + uint32_t(j & 1) * 128u;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kPanel + (kk & 3) * 32;
-                    mma_bf16_ss(d, smem_desc(qaddr + koff, 16, 1024), smem_desc(kaddr + koff, 16, 1024), kIdS,
-                                kk > 0);
+                    const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
+                    mma_bf16_ss(d, dq + koff, kb + koff, kIdS, kk > 0);
                 }
+                if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
+                else mma_commit_multicast(&bars->k_empty[stage], kMask);
                 mma_commit(&bars->s_full[j & 1]);
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait_bounded(&bars->p_full[j & 1], (j >> 1) & 1, kWaitNs)) return false;
-                tc_fence_after();
                 const int stage = j % kNS;
-                const uint32_t vaddr = sbase + kOffV + stage * kTile;
+                if (!mbar_wait_bounded(&bars->p_full[j & 1], (j >> 1) & 1, kWaitNs)) return false;
+                if (!mbar_wait_bounded(&bars->v_full[stage], (j / kNS) & 1, kWaitNs)) return false;
+                tc_fence_after();
+                const uint64_t vb = dv + uint64_t((stage * kTile) >> 4);
                 const uint32_t pcol = tbase + kColP + uint32_t(j & 1) * 64u;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {      // 16 tokens = 8 packed columns of P
-                    mma_bf16_ts(tbase + kColO, pcol + kk * 8, smem_desc(vaddr + kk * 2048, kPanel, 1024), kIdO,
+                    mma_bf16_ts(tbase + kColO, pcol + kk * 8, vb + uint64_t((kk * 2048) >> 4), kIdO,
                                 (j > 0 || kk > 0));
                 }
-                if constexpr (CL == 1) mma_commit(&bars->kv_empty[stage]);
-                else mma_commit_multicast(&bars->kv_empty[stage], kMask);
+                if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
+                else mma_commit_multicast(&bars->v_empty[stage], kMask);
                 mma_commit(&bars->p_free[j & 1]);
                 return true;
             };
             if (ok) ok = issue_s(0);
+            if (ok && ntiles > 1) ok = issue_s(1);
             for (int j = 0; ok && j < ntiles; ++j) {
                 if (*abort_flag) { ok = false; break; }
-                if (j + 1 < ntiles) ok = issue_s(j + 1);
+                if (j + 2 < ntiles) ok = issue_s(j + 2);
                 if (ok) ok = issue_pv(j);
             }
             if (!ok) {
