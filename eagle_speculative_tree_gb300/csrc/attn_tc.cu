@@ -4,20 +4,23 @@
 // computed with tcgen05:
 //   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
 //     are zero) x one split of the sequence's logical tokens, in 128-token tiles;
-//   * warp 0 streams the split's K pages and warp 10 its V pages with TMA (one
-//     16-token page x 64 head-dim columns per copy, 128-byte swizzle; lanes 0-7 issue
-//     one page each) into two three-stage rings; the partly filled last page of a
-//     sequence and pages past the split are written by the warp itself, zero-filled,
-//     so nothing outside the sequence reaches the MMA;
-//   * warp 1 allocates all 512 TMEM columns (S and P double-buffered, O) and issues
-//     S = Q K^T from shared memory and O += P V with P read from TMEM, as
-//     128x128x16 tcgen05.mma instructions;
+//   * warp 0 streams the split's K pages (four-stage ring) and warp 10 its V pages
+//     (three stages) with TMA (one 16-token page x 64 head-dim columns per copy,
+//     128-byte swizzle; lanes 0-7 issue one page each); the partly filled last page
+//     of a sequence and pages past the split are written by the warp itself,
+//     zero-filled, so nothing outside the sequence reaches the MMA;
+//   * TMEM (512 columns, allocated by warp 1) holds two S buffers, Q and O; P_j is
+//     written over S_j.  Warp 1 issues S = Q K^T with Q read from TMEM, warp 11 issues
+//     O += P V with P read from TMEM, both as 128x128x16 tcgen05.mma instructions (two
+//     issuers, so that the barrier waits of one stream overlap the other's MMAs).  Only
+//     K and V pass through shared memory, whose bandwidth the MMAs and TMA share;
 //   * warps 2-9 (two per TMEM lane quarter, one query row per thread, each warp one
-//     half of the tile's columns) read S from TMEM, apply the tree mask -- prefix tokens always, tree token S+j only when bit
-//     j of the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2
-//     mask M and section 5 bitmask) -- run the online softmax in base 2, write P as
-//     packed bf16 back to TMEM, and rescale O in TMEM only when a row's running max
-//     grows by more than 2^8.
+//     half of the tile's columns) stage Q into TMEM, then per tile read S from TMEM,
+//     apply the tree mask -- prefix tokens always, tree token S+j only when bit j of
+//     the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2 mask M
+//     and section 5 bitmask) -- run the online softmax in base 2, write P as packed
+//     bf16 back to TMEM, and rescale O in TMEM only when a row's running max grows by
+//     more than 2^8.
 // Every mbarrier wait is bounded; on expiry the CTA records TREESPEC_STATUS_TIMEOUT,
 // drains its own tensor-core work, frees TMEM and exits.
 #include <cuda.h>
@@ -35,38 +38,64 @@ using namespace sm100;
 constexpr int kM = 128;              // query rows per CTA = TMEM lanes
 constexpr int kD = 128;              // head dim
 constexpr int kBN = 128;             // tokens per tile
-constexpr int kNS = 3;               // K/V ring stages
+constexpr int kNSK = 4;              // K ring stages
+constexpr int kNSV = 3;              // V ring stages
 constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
 constexpr int kTile = 2 * kPanel;    // [128][128] bf16
-constexpr int kThreads = 352;        // K producer, MMA, 8 softmax warps, V producer
+constexpr int kThreads = 384;        // K producer, S issuer, 8 softmax warps, V producer, PV issuer
 constexpr int kWarpV = 10;           // the V producer warp
+constexpr int kWarpPV = 11;          // the P V issuer warp
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;        // S double buffer: columns [0, 256)
-constexpr uint32_t kColP = 256;      // P double buffer (bf16 pairs): [256, 384)
+constexpr int kSB = 2;               // S buffers in TMEM: columns [0, 256); P_j overwrites S_j
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColQ = 256;      // Q (bf16 pairs): [256, 320)
 constexpr uint32_t kColO = 384;      // O: [384, 512)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 // shared-memory map (offsets from a 1024-aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;
-constexpr int kOffV = kOffK + kNS * kTile;
-constexpr int kOffBar = kOffV + kNS * kTile;
-constexpr int kNumBars = 4 * kNS + 2 + 2 + 2 + 2 + 2;   // k/v full/empty, s_full/empty, p_full, p_free, q_full, drain
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kNSK * kTile;
+constexpr int kOffBar = kOffV + kNSV * kTile;
+constexpr int kNumBars = 2 * kNSK + 2 * kNSV + 3 * kSB + 1 + 2 + 8;   // k/v full/empty, s_full, p_full, s_free, q_full, drain x2, xchg
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffFlag = kOffMisc + 16;                     // exchange sequence numbers, 4 quarters x 2 halves
-constexpr int kOffXch = kOffFlag + 32;                      // softmax half-row exchange, 2 x 2 x 128 floats
+constexpr int kOffXch = kOffMisc + 16;                      // softmax half-row exchange, 2 x 2 x 128 floats
 constexpr int kOffAnc = kOffXch + 2 * 2 * 128 * 4;
-constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 232,160 bytes: within the 227 KB limit
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 232,200 bytes: within the 227 KB limit
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t k_full[kNS], k_empty[kNS], v_full[kNS], v_empty[kNS], s_full[2], s_empty[2], p_full[2], p_free[2], q_full, drain;
+    uint64_t k_full[kNSK], k_empty[kNSK], v_full[kNSV], v_empty[kNSV], s_full[kSB], p_full[kSB], s_free[kSB], q_full, drain[2], xchg[4][2];
 };
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (d0, d1) = (a0 * b + c, a1 * b + c) as one packed f32x2 instruction
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (d0, d1) += (a0, a1) as one packed f32x2 instruction
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
 }
 
 // CL > 1: the CL CTAs of a cluster hold consecutive row blocks of the same
@@ -115,22 +144,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (tid == 0) {
-        for (int s = 0; s < kNS; ++s) {
+        for (int s = 0; s < kNSK; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], CL);
+        }
+        for (int s = 0; s < kNSV; ++s) {
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], CL);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kSB; ++s) {
             mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->s_empty[s], 256);
             mbar_init(&bars->p_full[s], 256);
-            mbar_init(&bars->p_free[s], 1);
+            mbar_init(&bars->s_free[s], 1);
         }
         mbar_init(&bars->q_full, 256);
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain[0], 1);
+        mbar_init(&bars->drain[1], 1);
         *abort_flag = 0;
-        for (int f = 0; f < 8; ++f) reinterpret_cast<volatile int*>(sm + kOffFlag)[f] = 0;
+        for (int f = 0; f < 8; ++f) mbar_init(&bars->xchg[f >> 1][f & 1], 2);
         fence_mbar_init();
     }
     for (int e = tid; e < p.N; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N + e];
@@ -149,9 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kWarpV) {
         // ------------------------------------------------------------ TMA producers
-        // warp 0 streams K, warp 10 streams V: a K stage is free again as soon as S of
-        // its tile has been computed, a V stage only after P V, so each has its own ring.
+        // warp 0 streams K (4 stages), warp 10 streams V (3 stages): a K stage is free again
+        // as soon as S of its tile has been computed, a V stage only after P V.
         const bool is_v = warp == kWarpV;
+        const int nst = is_v ? kNSV : kNSK;                 // ring stages
         uint64_t* full = is_v ? bars->v_full : bars->k_full;
         uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
         const uint16_t* src = static_cast<const uint16_t*>(is_v ? p.v : p.k);
@@ -159,16 +191,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char* ring = sm + (is_v ? kOffV : kOffK);
         const int* ptab = p.page_table + size_t(b) * p.max_pages;
         if (lane == 0) tma_prefetch_desc(map);
-        // page ids of tile j (lane k < 8 holds page k of the tile), fetched one tile ahead
-        auto fetch_pages = [&](int j) -> int {
-            const int pos0 = t0 + j * kBN + lane * 16;
-            return (lane < 8 && j < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
+        // Page ids in batches of four tiles, one warp-wide load each (lane l: page l & 7 of
+        // tile 4 * batch + (l >> 3)), fetched a whole batch ahead: a page-table read that
+        // waits behind the K/V traffic in L2 then never holds up the ring.
+        auto fetch_batch = [&](int bi) -> int {
+            const int jt = 4 * bi + (lane >> 3);
+            const int pos0 = t0 + jt * kBN + (lane & 7) * 16;
+            return (jt < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
         };
-        int page_next = fetch_pages(0);
+        int batch_cur = fetch_batch(0), batch_next = fetch_batch(1);
         for (int j = 0; j < ntiles; ++j) {
-            const int stage = j % kNS;
-            int page = page_next;
-            page_next = fetch_pages(j + 1);
+            const int stage = j % nst;
+            if (j > 0 && (j & 3) == 0) {
+                batch_cur = batch_next;
+                batch_next = fetch_batch((j >> 2) + 1);
+            }
+            int page = __shfl_sync(0xffffffffu, batch_cur, ((j & 3) << 3) | (lane & 7));
             const int base = t0 + j * kBN;
             // lanes 0..7 own page `lane` of the tile: 1 = full page by TMA, 2 = written here
             // (the sequence's partly filled last page, a bad page id, or past the split)
@@ -185,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     page = -1;
                 }
             }
-            if (j >= kNS && !mbar_wait_bounded(&empty[stage], ((j / kNS) - 1) & 1, kWaitNs)) {
+            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, kWaitNs)) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
             }
@@ -228,75 +266,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (CL > 1) {
             // every peer's release of every stage has landed here before this CTA may exit
-            for (int s2 = 0; s2 < kNS && s2 < ntiles; ++s2) {
-                const int uses = (ntiles - s2 + kNS - 1) / kNS;
+            for (int s2 = 0; s2 < nst && s2 < ntiles; ++s2) {
+                const int uses = (ntiles - s2 + nst - 1) / nst;
                 if (!mbar_wait_bounded(&empty[s2], (uses - 1) & 1, kWaitNs)) {
                     *abort_flag = 1;
                     atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Order S_0, S_1, then S_{j+2} before P_j V_j: the next scores are already queued
-        // when the softmax hands over P_j, so the softmax warps never wait for S.
+    } else if (warp == 1 || warp == kWarpPV) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two independent streams into the CTA's tensor pipe: warp 1 issues S_j = Q K_j^T,
+        // warp 11 issues O += P_j V_j.  They share no TMEM columns and no ring, so the
+        // barrier waits of one overlap the other's MMAs instead of draining the pipe.
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
-            constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
-            // descriptors of the first K-step of Q, of ring stage 0 of K and of V; a
-            // step or a stage moves only the start-address field (address >> 4 in the
-            // low 14 bits, which no offset inside the 227 KB window overflows)
-            const uint64_t dq = smem_desc(sbase + kOffQ, 16, 1024);
-            const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
-            const uint64_t dv = smem_desc(sbase + kOffV, kPanel, 1024);
-            bool ok = mbar_wait_bounded(&bars->q_full, 0, kWaitNs);
-            auto issue_s = [&](int j) -> bool {
-                const int stage = j % kNS;
-                if (!mbar_wait_bounded(&bars->k_full[stage], (j / kNS) & 1, kWaitNs)) return false;
-                if (j >= 2 && !mbar_wait_bounded(&bars->s_empty[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) return false;
-                tc_fence_after();
-                const uint64_t kb = dk + uint64_t((stage * kTile) >> 4);
-                const uint32_t d = tbase + kColS + uint32_t(j & 1) * 128u;
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
-                    mma_bf16_ss(d, dq + koff, kb + koff, kIdS, kk > 0);
-                }
-                if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
-                else mma_commit_multicast(&bars->k_empty[stage], kMask);
-                mma_commit(&bars->s_full[j & 1]);
-                return true;
+            const bool pv = warp == kWarpPV;
+            // both barriers of a step tested back to back, then waited (bounded) if needed
+            auto ready2 = [&](uint64_t* x, uint32_t px, uint64_t* y, uint32_t py) -> bool {
+                const bool rx = mbar_try_wait(x, px);
+                const bool ry = mbar_try_wait(y, py);
+                if (rx && ry) return true;
+                if (*abort_flag) return false;
+                return (rx || mbar_wait_bounded(x, px, kWaitNs)) && (ry || mbar_wait_bounded(y, py, kWaitNs));
             };
-            auto issue_pv = [&](int j) -> bool {
-                const int stage = j % kNS;
-                if (!mbar_wait_bounded(&bars->p_full[j & 1], (j >> 1) & 1, kWaitNs)) return false;
-                if (!mbar_wait_bounded(&bars->v_full[stage], (j / kNS) & 1, kWaitNs)) return false;
-                tc_fence_after();
-                const uint64_t vb = dv + uint64_t((stage * kTile) >> 4);
-                const uint32_t pcol = tbase + kColP + uint32_t(j & 1) * 64u;
+            bool ok = true;
+            if (!pv) {
+                constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
+                // Q is read from TMEM (written there by the softmax warps), K from the ring;
+                // a K-step or a stage moves only the start-address field of the K descriptor
+                // (address >> 4 in the low 14 bits, which no offset in the window overflows)
+                const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
+                ok = mbar_wait_bounded(&bars->q_full, 0, kWaitNs);
+                for (int j = 0; ok && j < ntiles; ++j) {
+                    const int stage = j % kNSK;
+                    // K_j has landed; S buffer j%2 is free once P_{j-2} V_{j-2} has read it
+                    const int sb = j % kSB;
+                    ok = j >= kSB ? ready2(&bars->k_full[stage], (j / kNSK) & 1, &bars->s_free[sb], ((j / kSB) - 1) & 1)
+                                  : mbar_wait_bounded(&bars->k_full[stage], (j / kNSK) & 1, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t kb = dk + uint64_t((stage * kTile) >> 4);
+                    const uint32_t d = tbase + kColS + uint32_t(sb) * 128u;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {      // 16 tokens = 8 packed columns of P
-                    mma_bf16_ts(tbase + kColO, pcol + kk * 8, vb + uint64_t((kk * 2048) >> 4), kIdO,
-                                (j > 0 || kk > 0));
+                    for (int kk = 0; kk < kD / 16; ++kk) {       // 16 head dims = 8 packed columns of Q
+                        const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
+                        mma_bf16_ts(d, tbase + kColQ + kk * 8, kb + koff, kIdS, kk > 0);
+                    }
+                    if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
+                    else mma_commit_multicast(&bars->k_empty[stage], kMask);
+                    mma_commit(&bars->s_full[sb]);
                 }
-                if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
-                else mma_commit_multicast(&bars->v_empty[stage], kMask);
-                mma_commit(&bars->p_free[j & 1]);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && ntiles > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                if (*abort_flag) { ok = false; break; }
-                if (j + 2 < ntiles) ok = issue_s(j + 2);
-                if (ok) ok = issue_pv(j);
+            } else {
+                constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
+                const uint64_t dv = smem_desc(sbase + kOffV, kPanel, 1024);
+                for (int j = 0; ok && j < ntiles; ++j) {
+                    const int stage = j % kNSV;
+                    // P_j is in TMEM; V_j has landed
+                    const int sb = j % kSB;
+                    ok = ready2(&bars->p_full[sb], (j / kSB) & 1, &bars->v_full[stage], (j / kNSV) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t vb = dv + uint64_t((stage * kTile) >> 4);
+                    // P_j sits in S_j's buffer: tokens 0-63 in columns [0, 32), tokens 64-127 in
+                    // [64, 96) (each softmax warp overwrites only its own half of S)
+                    const uint32_t pcol = tbase + kColS + uint32_t(sb) * 128u;
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {      // 16 tokens = 8 packed columns of P
+                        mma_bf16_ts(tbase + kColO, pcol + (kk >> 2) * 64 + (kk & 3) * 8, vb + uint64_t((kk * 2048) >> 4),
+                                    kIdO, (j > 0 || kk > 0));
+                    }
+                    if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
+                    else mma_commit_multicast(&bars->v_empty[stage], kMask);
+                    mma_commit(&bars->s_free[sb]);
+                }
             }
             if (!ok) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
             }
-            mma_commit(&bars->drain);                        // everything issued above has finished
-            mbar_wait_bounded(&bars->drain, 0, kWaitNs);
+            uint64_t* drain = &bars->drain[pv ? 1 : 0];
+            mma_commit(drain);                               // everything this thread issued has finished
+            mbar_wait_bounded(drain, 0, kWaitNs);
         }
         __syncwarp();
     } else {
@@ -314,47 +364,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t anc = row_ok ? anc_s[i] : 0ull;
         const bool warp_rows = __any_sync(0xffffffffu, row_ok);
         const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
-        volatile float* xch = reinterpret_cast<volatile float*>(sm + kOffXch);  // [2 parity][2 half][128 rows]
-        volatile int* flags = reinterpret_cast<volatile int*>(sm + kOffFlag);   // [4 quarter][2 half]
-        // Swap one float per row with the other half's warp of this quarter: publish the
-        // value, then the sequence number; wait (bounded) for the partner's number.  Two
-        // parity slots: slot seq&1 is rewritten only after the partner has moved past seq.
-        auto exchange = [&](float value, int seq, bool* ok) -> float {
+        float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2 slot][2 half][128 rows]
+        // Swap one float per row with the other half's warp of this quarter (both sit on
+        // the same scheduler): write the value, arrive on the quarter's barrier of slot
+        // seq&1 (two arrivals per phase); collect waits for that phase, sleeping in
+        // hardware, and reads the partner's value.  Slot seq&1 is rewritten at seq+2 only
+        // after the partner's arrival for seq+1, which follows its collect of seq.
+        auto publish = [&](float value, int seq) {
             xch[((seq & 1) * 2 + half) * 128 + t] = value;
-            __threadfence_block();
             __syncwarp();
-            if (lane == 0) flags[quarter * 2 + half] = seq;
-            bool good = true;
-            if (lane == 0 && flags[quarter * 2 + (half ^ 1)] < seq) {
-                const uint64_t t_start = global_ns();
-                while (flags[quarter * 2 + (half ^ 1)] < seq) {
-                    if (global_ns() - t_start > kWaitNs) { good = false; break; }
-                }
-            }
-            good = __shfl_sync(0xffffffffu, good, 0);
-            __threadfence_block();
-            *ok = good;
+            if (lane == 0) mbar_arrive(&bars->xchg[quarter][seq & 1]);
+        };
+        auto collect = [&](int seq, bool* ok) -> float {
+            *ok = mbar_wait_bounded(&bars->xchg[quarter][seq & 1], ((seq - 1) >> 1) & 1, kWaitNs);
             return xch[((seq & 1) * 2 + (half ^ 1)) * 128 + t];
         };
         {
+            // this row's 64 head dims of Q into TMEM as 32 bf16 pairs (the A operand of S)
             const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                                ((size_t(b) * p.N + i) * p.Hq + hq) * kD) + half * 8;
+            uint32_t qv[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint4 v = row_ok ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + kOffQ + half * kPanel + sw128_offset(t, c)) = v;
+                const uint4 w = row_ok ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
+                qv[4 * c] = w.x;
+                qv[4 * c + 1] = w.y;
+                qv[4 * c + 2] = w.z;
+                qv[4 * c + 3] = w.w;
             }
+            tmem_st32(tl + kColQ + half * 32, qv);
+            tmem_wait_st();
         }
-        fence_proxy_async_smem();
+        tc_fence_before();
         mbar_arrive(&bars->q_full);
 
         const float sc = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;                   // l: this warp's half of the row sum
         bool alive = true;
+        uint32_t v[kBN / 2];
         for (int j = 0; j < ntiles && alive; ++j) {
             const int base = t0 + j * kBN;
-            if (!mbar_wait_bounded(&bars->s_full[j & 1], (j >> 1) & 1, kWaitNs)) { alive = false; break; }
-            tc_fence_after();
             // which of this half's 64 columns the row may see, as two 32-bit words: prefix
             // columns below pref_end, tree columns [tree_lo, tree_hi) via the ancestor word
             const int pref_end = min(S, t1) - base;
@@ -375,56 +424,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mw[w] = row_ok ? bits : 0u;
             }
             const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
-            uint32_t v[kBN / 2];
-            if (warp_rows) {
-                tmem_ld32(tl + kColS + uint32_t(j & 1) * 128u + half * 64, v);
-                tmem_ld32(tl + kColS + uint32_t(j & 1) * 128u + half * 64 + 32, v + 32);
-                tmem_wait_ld();
-            }
-            tc_fence_before();
-            mbar_arrive(&bars->s_empty[j & 1]);            // S buffer reusable from here
-            constexpr uint32_t kNegInf = 0xff800000u;
-            if (!full) {
+            const int sb = j % kSB;
+            const uint32_t scol = tl + kColS + uint32_t(sb) * 128u + half * 64;
+            // S of this half-row into v, masked columns set to -inf
+            auto load_s = [&]() {
+                if (warp_rows) {
+                    tmem_ld32(scol, v);
+                    tmem_ld32(scol + 32, v + 32);
+                    tmem_wait_ld();
+                }
+                constexpr uint32_t kNegInf = 0xff800000u;
+                if (!full) {
 #pragma unroll
-                for (int c = 0; c < kBN / 2; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
-            }
+                    for (int c = 0; c < kBN / 2; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
+                }
+            };
+            // probabilities 2^(s*scale - msub), rounded to bf16 and packed in pairs in place
+            // (pair c overwrites v[c], whose value was read at pair c/2); returns their sum
+            auto exps = [&](float msub) -> float {
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+                for (int c = 0; c < kBN / 4; ++c) {
+                    float x0, x1;
+                    fma_f32x2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), sc, -msub);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    v[c] = pack_bf16x2(p0, p1);
+                    if (c & 1) add_f32x2(a2, a3, p0, p1);
+                    else add_f32x2(a0, a1, p0, p1);
+                }
+                return (a0 + a1) + (a2 + a3);
+            };
+            if (!mbar_wait_bounded(&bars->s_full[sb], (j / kSB) & 1, kWaitNs)) { alive = false; break; }
+            tc_fence_after();
+            load_s();
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kBN / 2; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
-            float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            for (int c = 0; c < kBN / 2; c += 8) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    mx[e] = fmax3(mx[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
+            }
+            const float mhalf = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+            publish(mhalf, j + 1);
+            // Speculate that the running max stays: the exponentials taken now are final
+            // unless some row's max over both halves rises more than 8 above m_used.
+            const bool spec = __all_sync(0xffffffffu, mhalf * sc <= m_used + 8.f);
+            float lsum = 0.f;
+            if (spec) lsum = exps(m_used == -INFINITY ? 0.f : m_used);
             // the row's max over both halves (identical in the two warps of the quarter)
             bool xok = true;
-            mraw = fmaxf(mraw, exchange(mraw, j + 1, &xok));
+            const float mt = fmaxf(mhalf, collect(j + 1, &xok)) * sc;   // scale > 0 commutes with max
             if (!xok) { alive = false; break; }
-            const float mt = mraw * sc;                    // scale > 0 commutes with max
             bool resc = false;
             float alpha = 1.f;
-            if (mt > m_used + 8.f) {
+            const bool grow = mt > m_used + 8.f;
+            if (grow) {
                 alpha = ex2(m_used - mt);
                 resc = m_used != -INFINITY;
                 l *= alpha;
                 m_used = mt;
             }
-            const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-            // probabilities 2^(s*scale - m), rounded to bf16 and packed in pairs in place
-            uint32_t* pk = v;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < kBN / 4; ++c) {
-                const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, -msub));
-                const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, -msub));
-                pk[c] = pack_bf16x2(p0, p1);
-                ls[c & 3] += p0 + p1;
+            if (!spec || __any_sync(0xffffffffu, grow)) {
+                if (spec) load_s();                        // v holds P: S is still in TMEM
+                lsum = exps(m_used == -INFINITY ? 0.f : m_used);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            // P buffer j&1 is free once P_{j-2} V_{j-2} has completed
-            if (j >= 2 && !mbar_wait_bounded(&bars->p_free[j & 1], ((j - 2) >> 1) & 1, kWaitNs)) {
-                alive = false;
-                break;
-            }
+            l += lsum;
             if (__any_sync(0xffffffffu, resc)) {
                 // O may only be rescaled once P_{j-1} V_{j-1} is in it (this warp's 64 columns)
-                if (!mbar_wait_bounded(&bars->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1, kWaitNs)) {
+                if (!mbar_wait_bounded(&bars->s_free[(j - 1) % kSB], ((j - 1) / kSB) & 1, kWaitNs)) {
                     alive = false;
                     break;
                 }
@@ -441,19 +508,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_after();
-            if (warp_rows) tmem_st32(tl + kColP + uint32_t(j & 1) * 64u + half * 32, pk);
+            if (warp_rows) tmem_st32(scol, v);             // P over the first 32 columns of this half of S
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[j & 1]);
+            mbar_arrive(&bars->p_full[sb]);
         }
         if (!alive) {
             *abort_flag = 1;
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-        } else if (mbar_wait_bounded(&bars->p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, kWaitNs)) {
+        } else if (mbar_wait_bounded(&bars->s_free[(ntiles - 1) % kSB], ((ntiles - 1) / kSB) & 1, kWaitNs)) {
             tc_fence_after();
             // the row sum over both halves
             bool xok = true;
-            const float lrow = l + exchange(l, ntiles + 1, &xok);
+            publish(l, ntiles + 1);
+            const float lrow = l + collect(ntiles + 1, &xok);
             if (!xok) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
@@ -562,7 +630,11 @@ cudaError_t launch_cluster(const AttnParams& p, const CUtensorMap& mk, const CUt
     return cudaGetLastError();
 }
 
-int attn_tc_cluster_size(int row_blocks) { return row_blocks % 4 == 0 ? 4 : row_blocks % 2 == 0 ? 2 : 1; }
+// Pairs of row blocks of one kv head share each K/V copy (multicast): half the L2 reads
+// and TMA copies per CTA.  Clusters of 4 fit only 144 of the 152 SMs (whole GPCs),
+// clusters of 2 all of them.  Measured on 32 x 8192-token sequences (64 q / 8 kv heads,
+// 64 tree nodes): 0.532 ms without clusters, 0.493 ms with pairs, 0.60 ms with 4.
+int attn_tc_cluster_size(int row_blocks) { return row_blocks % 2 == 0 ? 2 : 1; }
 
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
     CUtensorMap mk, mv;
