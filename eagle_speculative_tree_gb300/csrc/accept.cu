@@ -40,6 +40,11 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Ask the L2 for the 128-byte line holding `p` (no data comes back to the thread).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Softmax probability of one logit, evaluated identically everywhere:
 // p = 2^(logit * c - M2) / S with c = log2(e) / T and M2 = max(logit * c).
 __device__ __forceinline__ float prob_at(float logit, float c, float M2, float invS) {
@@ -79,6 +84,22 @@ __device__ __forceinline__ double block_sum_d(double v, double* red) {
     if (warp == 0) {
         double t = lane < NT / 32 ? red[lane] : 0.0;
         t = warp_sum_d(t);
+        if (lane == 0) red[0] = t;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+template <int NT>
+__device__ __forceinline__ float block_sum_f(float v, float* red) {
+    v = warp_sum(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float t = lane < NT / 32 ? red[lane] : 0.f;
+        t = warp_sum(t);
         if (lane == 0) red[0] = t;
     }
     __syncthreads();
@@ -619,6 +640,17 @@ struct ClusterReducer {
         phase ^= 1;
         return t;
     }
+    // float sum (partials combined in rank order, so every CTA gets the same value)
+    __device__ float sumf(float v) {
+        cg::cluster_group cl = cg::this_cluster();
+        v = block_sum_f<NT>(v, redf);
+        if (threadIdx.x == 0) cr->f[phase][cl.block_rank()] = v;
+        cl.sync();
+        float t = 0.f;
+        for (int k = 0; k < CL; ++k) t += cl.map_shared_rank(cr, k)->f[phase][k];
+        phase ^= 1;
+        return t;
+    }
     __device__ float max(float v) {
         cg::cluster_group cl = cg::this_cluster();
         v = block_max_f<NT>(v, redf);
@@ -697,11 +729,14 @@ __device__ __forceinline__ double block_exclusive_d(double v, double* scratch) {
 template <int CL, int NT, int E, bool STOCH>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_cluster_kernel(AcceptParams p) {
     __shared__ int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
-    __shared__ float izs[kMaxNodes];
+    __shared__ float izs[kMaxNodes], uni[kMaxNodes];
     __shared__ double redd[32], scan[NT / 32 + 1];
     __shared__ float redf[32];
     __shared__ int redi[32];
-    __shared__ int s_cur, s_len, s_action, s_child, s_found;
+    __shared__ int s_cur, s_len, s_action, s_child, s_found, s_cv0, s_chit;
+    __shared__ float ch_lg[kMaxNodes], ch_q[kMaxNodes];     // target logit / draft prob of each child's token
+    __shared__ float cw[E];                                  // the crossing thread's bonus weights
+    __shared__ double s_cbase;
     __shared__ ClusterRed<CL> cred;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
@@ -713,6 +748,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     for (int c = tid; c < N; c += NT) {
         par[c] = p.parents[size_t(b) * N + c];
         tok[c] = p.tokens[size_t(b) * N + c];
+        if (STOCH) uni[c] = p.uniforms[size_t(b) * N + c];
     }
     if (tid == 0) {
         s_cur = 0;
@@ -721,7 +757,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     __syncthreads();
     uint32_t st = (tid == 0 && rank == 0) ? check_parents(par, N) : 0u;
 
-    float r[E], qv[E];
+    float r[E];
+    // the draft row is read only where a child is rejected (and for the bonus draw), from
+    // L1/L2, instead of being held in registers beside the target row
+    auto q_at = [&](const float* q, int e) -> float4 {
+        const int v = v0 + e;
+        return v < V ? __ldg(reinterpret_cast<const float4*>(q + v)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    const float* q_last = nullptr;                          // the draft row of the last visited node
     int amax = 0, rej = 0;
     float M2 = 0.f, invS = 1.f;
     for (int depth = 0; depth < N; ++depth) {
@@ -729,17 +772,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         const size_t row = size_t(b) * N + cur;
         const float* lg = p.logits + row * V;
         const float* qr = STOCH ? p.probs + row * V : nullptr;
+        q_last = qr;
+        if (STOCH && v0 < V) {                              // this thread's draft tokens, into L2 early
+#pragma unroll
+            for (int e = 0; e < E; e += 32) prefetch_line_l2(qr + v0 + e);
+        }
+        if (STOCH) {                                        // what the sibling tests below will need
+            for (int c = tid; c < N; c += NT) {
+                const int x = tok[c];
+                if (par[c] == cur && x >= 0 && x < V) {
+                    ch_lg[c] = __ldg(lg + x);
+                    ch_q[c] = __ldg(qr + x);
+                }
+            }
+        }
+        float piz = 0.f;                                    // a rescale of r still to apply (0: none)
 #pragma unroll
         for (int e = 0; e < E; e += 4) {
             const int v = v0 + e;
             float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (v < V) {
-                x = __ldg(reinterpret_cast<const float4*>(lg + v));
-                if (STOCH) y = __ldg(reinterpret_cast<const float4*>(qr + v));
-            }
+            if (v < V) x = __ldg(reinterpret_cast<const float4*>(lg + v));
             r[e] = x.x; r[e + 1] = x.y; r[e + 2] = x.z; r[e + 3] = x.w;
-            qv[e] = y.x; qv[e + 1] = y.y; qv[e + 2] = y.z; qv[e + 3] = y.w;
         }
         if constexpr (!STOCH) {
             float best = -INFINITY;
@@ -759,7 +812,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                 r[e] = ex2(fmaf(r[e], p.c, -M2));                 // -inf (padding) -> 0
                 ls[e & 3] += r[e];
             }
-            invS = 1.f / float(red.sum((double(ls[0]) + double(ls[1])) + (double(ls[2]) + double(ls[3]))));
+            invS = 1.f / red.sumf((ls[0] + ls[1]) + (ls[2] + ls[3]));
 #pragma unroll
             for (int e = 0; e < E; ++e) r[e] *= invS;               // r = p, as prob_at
         }
@@ -779,9 +832,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                         if (!STOCH) {
                             ok = x == amax;
                         } else {
-                            const float qx = __ldg(qr + x);
-                            const float rx = residual_at(prob_at(__ldg(lg + x), p.c, M2, invS), qx, izs, jj);
-                            ok = rx > 0.f && p.uniforms[size_t(b) * N + nc] * qx <= rx;
+                            const float qx = ch_q[nc];
+                            const float rx = residual_at(prob_at(ch_lg[nc], p.c, M2, invS), qx, izs, jj);
+                            ok = rx > 0.f && uni[nc] * qx <= rx;
                         }
                     }
                     if (ok) {
@@ -804,22 +857,42 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             ++jj;
             if (action == 3) break;
             if constexpr (STOCH) {                          // the next sibling sees the residual
+                // the previous sibling's rescale r = max(r - q, 0) / Z is applied here, in the
+                // same pass over q as this residual's mass (same operations, one read of q)
                 float zs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < E; ++e) zs4[e & 3] += fmaxf(r[e] - qv[e], 0.f);
-                const double Z = red.sum((double(zs4[0]) + double(zs4[1])) + (double(zs4[2]) + double(zs4[3])));
-                const float iz = float(Z) > 0.f ? 1.f / float(Z) : 0.f;
-                if (tid == 0) izs[jj - 1] = iz;
-                if (iz > 0.f) {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) r[e] = fmaxf(r[e] - qv[e], 0.f) * iz;
+                for (int e = 0; e < E; e += 4) {
+                    const float4 q4 = q_at(qr, e);
+                    if (piz > 0.f) {
+                        r[e] = fmaxf(r[e] - q4.x, 0.f) * piz;
+                        r[e + 1] = fmaxf(r[e + 1] - q4.y, 0.f) * piz;
+                        r[e + 2] = fmaxf(r[e + 2] - q4.z, 0.f) * piz;
+                        r[e + 3] = fmaxf(r[e + 3] - q4.w, 0.f) * piz;
+                    }
+                    zs4[0] += fmaxf(r[e] - q4.x, 0.f);
+                    zs4[1] += fmaxf(r[e + 1] - q4.y, 0.f);
+                    zs4[2] += fmaxf(r[e + 2] - q4.z, 0.f);
+                    zs4[3] += fmaxf(r[e + 3] - q4.w, 0.f);
                 }
-                __syncthreads();
+                const float Z = red.sumf((zs4[0] + zs4[1]) + (zs4[2] + zs4[3]));
+                const float iz = Z > 0.f ? 1.f / Z : 0.f;
+                if (tid == 0) izs[jj - 1] = iz;
+                piz = iz;
             }
             pos = child;
         }
         if (action != 1) {
             rej = jj;
+            if (STOCH && piz > 0.f) {                       // the last deferred rescale
+#pragma unroll
+                for (int e = 0; e < E; e += 4) {
+                    const float4 q4 = q_at(qr, e);
+                    r[e] = fmaxf(r[e] - q4.x, 0.f) * piz;
+                    r[e + 1] = fmaxf(r[e + 1] - q4.y, 0.f) * piz;
+                    r[e + 2] = fmaxf(r[e + 2] - q4.z, 0.f) * piz;
+                    r[e + 3] = fmaxf(r[e + 3] - q4.w, 0.f) * piz;
+                }
+            }
             break;
         }
         if (tid == 0) {
@@ -837,17 +910,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         if (!STOCH && tid == 0) p.bonus[b] = amax;
     }
     if constexpr (STOCH) {
-        // bonus token: inverse CDF of r_rej (up to normalisation) in token order
-        float w[E];
+        // bonus token: inverse CDF of r_rej (up to normalisation) in token order; the weights
+        // w = r (no rejection at this node, or zero residual mass) or max(r - q, 0)
         bool unchanged = false;
+        auto weight4 = [&](int e) -> float4 {
+            if (rej == 0 || unchanged) return make_float4(r[e], r[e + 1], r[e + 2], r[e + 3]);
+            const float4 q4 = q_at(q_last, e);
+            return make_float4(fmaxf(r[e] - q4.x, 0.f), fmaxf(r[e + 1] - q4.y, 0.f), fmaxf(r[e + 2] - q4.z, 0.f),
+                               fmaxf(r[e + 3] - q4.w, 0.f));
+        };
         double total = 0.0, mine = 0.0;
         for (int attempt = 0; attempt < 2; ++attempt) {
-            mine = 0.0;
+            float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                w[e] = (rej == 0 || unchanged) ? r[e] : fmaxf(r[e] - qv[e], 0.f);
-                mine += double(w[e]);
+            for (int e = 0; e < E; e += 4) {
+                const float4 w4 = weight4(e);
+                m4[0] += w4.x;
+                m4[1] += w4.y;
+                m4[2] += w4.z;
+                m4[3] += w4.w;
             }
+            mine = double((m4[0] + m4[1]) + (m4[2] + m4[3]));
             total = red.sum(mine);
             if (total > 0.0 || rej == 0 || unchanged) break;
             unchanged = true;                                // zero residual mass: keep r_{rej-1}
@@ -860,21 +943,57 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         cta_total = scan[NT / 32];
         double all = 0.0;
         const double pre_cta = red.exclusive(cta_total, &all);
-        const double thr = double(p.uniforms[size_t(b) * N]) * total;
+        const double thr = double(uni[0]) * total;
         const double base = pre_cta + pre_thread;
         if (tid == 0 && rank == 0) s_found = 0;
+        if (tid == 0) s_chit = 0;
         cluster.sync();
         if (base <= thr && thr < base + mine) {              // the crossing lies in this thread's tokens
-            double run = base;
-            int v = -1, last_nz = -1;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                if (w[e] > 0.f) last_nz = v0 + e;
-                run += double(w[e]);
-                if (v < 0 && run > thr) v = v0 + e;
+            for (int e = 0; e < E; e += 4) {
+                const float4 w4 = weight4(e);
+                cw[e] = w4.x;
+                cw[e + 1] = w4.y;
+                cw[e + 2] = w4.z;
+                cw[e + 3] = w4.w;
             }
-            p.bonus[b] = v >= 0 ? v : last_nz;
-            *cluster.map_shared_rank(&s_found, 0) = 1;
+            s_cbase = base;
+            s_cv0 = v0;
+            s_chit = 1;
+        }
+        __syncthreads();
+        if (s_chit && tid < 32) {
+            // warp 0 walks those tokens: lane l holds E/32 of them, in token order
+            constexpr int PL = E / 32;
+            double sl = 0.0;
+            int lnz = -1;
+#pragma unroll
+            for (int u = 0; u < PL; ++u) {
+                const float w = cw[tid * PL + u];
+                sl += double(w);
+                if (w > 0.f) lnz = s_cv0 + tid * PL + u;
+            }
+            const double incl = warp_inclusive_scan_d(sl);
+            const unsigned pass = __ballot_sync(0xffffffffu, s_cbase + incl > thr);
+            int v = -1;
+            if (pass) {
+                const int L = __ffs(pass) - 1;
+                if (tid == L) {
+                    double run = s_cbase + (incl - sl);
+#pragma unroll
+                    for (int u = 0; u < PL; ++u) {
+                        run += double(cw[tid * PL + u]);
+                        if (v < 0 && run > thr) v = s_cv0 + tid * PL + u;
+                    }
+                }
+                v = __shfl_sync(0xffffffffu, v, L);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lnz = max(lnz, __shfl_xor_sync(0xffffffffu, lnz, o));
+            if (tid == 0) {
+                p.bonus[b] = v >= 0 ? v : lnz;
+                *cluster.map_shared_rank(&s_found, 0) = 1;
+            }
         }
         cluster.sync();
         if (rank == 0 && tid == 0 && s_found == 0) s_found = 2;     // nobody: rounding at the top end
@@ -883,8 +1002,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         if (none) {
             int last_nz = -1;
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                if (w[e] > 0.f) last_nz = v0 + e;
+            for (int e = 0; e < E; e += 4) {
+                const float4 w4 = weight4(e);
+                if (w4.x > 0.f) last_nz = v0 + e;
+                if (w4.y > 0.f) last_nz = v0 + e + 1;
+                if (w4.z > 0.f) last_nz = v0 + e + 2;
+                if (w4.w > 0.f) last_nz = v0 + e + 3;
+            }
             const int ln = red.argmax(float(last_nz), last_nz);  // largest index with mass
             if (rank == 0 && tid == 0) p.bonus[b] = ln < 0 ? 0 : ln;
         }
@@ -911,16 +1035,18 @@ template <bool STOCH>
 int launch_schedule(const AcceptParams& p, int mode, cudaStream_t s) {
     if (mode == TREESPEC_ACCEPT_PATH_ONLY) {
         const bool vec = p.V % 4 == 0 && p.B <= 65535;
+        // A row per cluster, 64 tokens per thread: clusters of 2 (76 fit on the GPU at
+        // once) up to 65,536 tokens, of 4 (36 at once) up to 131,072.
         if (vec && p.V > 16384 && p.V <= 32768) {
             accept_cluster_kernel<2, 512, 32, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
             return 1;
         }
         if (vec && p.V > 32768 && p.V <= 65536) {
-            accept_cluster_kernel<4, 512, 32, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
+            accept_cluster_kernel<2, 512, 64, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
             return 1;
         }
         if (vec && p.V > 65536 && p.V <= 131072) {
-            accept_cluster_kernel<8, 512, 32, STOCH><<<dim3(8, p.B), 512, 0, s>>>(p);
+            accept_cluster_kernel<4, 512, 64, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
             return 1;
         }
         if (p.V >= 32768) path_launch<512, STOCH>(p, s);
