@@ -64,7 +64,7 @@ def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "eagle_speculative_tree_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("attn_") or f in ("common.cuh", "tree_mask.cu"):
+        if f.startswith("attn_") or f in ("common.cuh", "sm100.cuh", "tree_mask.cu"):
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
