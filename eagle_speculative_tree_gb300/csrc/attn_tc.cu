@@ -279,15 +279,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Two independent streams into the CTA's tensor pipe: warp 1 issues S_j = Q K_j^T,
         // warp 11 issues O += P_j V_j.  They share no TMEM columns and no ring, so the
         // barrier waits of one overlap the other's MMAs instead of draining the pipe.
-        if (lane == 0) {
+        // The whole warp runs the loop (all lanes wait, so control flow stays uniform) and
+        // one elected lane issues each group of MMAs with its commits.  Each scheduler also
+        // runs two busy softmax warps: issue code in a one-lane branch measured 108 cycles
+        // per 128x128x16 MMA beside them, the warp-uniform form 69 (64 alone).
+        {
             const bool pv = warp == kWarpPV;
-            // both barriers of a step tested back to back, then waited (bounded) if needed
+            // both barriers of a step tested back to back, then waited (bounded) if needed;
+            // the verdict is made warp-uniform
             auto ready2 = [&](uint64_t* x, uint32_t px, uint64_t* y, uint32_t py) -> bool {
                 const bool rx = mbar_try_wait(x, px);
                 const bool ry = mbar_try_wait(y, py);
-                if (rx && ry) return true;
-                if (*abort_flag) return false;
-                return (rx || mbar_wait_bounded(x, px, kWaitNs)) && (ry || mbar_wait_bounded(y, py, kWaitNs));
+                bool r = rx && ry;
+                if (!__all_sync(0xffffffffu, r)) {
+                    r = !*abort_flag && (rx || mbar_wait_bounded(x, px, kWaitNs)) &&
+                        (ry || mbar_wait_bounded(y, py, kWaitNs));
+                }
+                return __all_sync(0xffffffffu, r);
             };
             bool ok = true;
             if (!pv) {
@@ -296,25 +304,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // a K-step or a stage moves only the start-address field of the K descriptor
                 // (address >> 4 in the low 14 bits, which no offset in the window overflows)
                 const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
-                ok = mbar_wait_bounded(&bars->q_full, 0, kWaitNs);
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->q_full, 0, kWaitNs));
                 for (int j = 0; ok && j < ntiles; ++j) {
                     const int stage = j % kNSK;
                     // K_j has landed; S buffer j%2 is free once P_{j-2} V_{j-2} has read it
                     const int sb = j % kSB;
                     ok = j >= kSB ? ready2(&bars->k_full[stage], (j / kNSK) & 1, &bars->s_free[sb], ((j / kSB) - 1) & 1)
-                                  : mbar_wait_bounded(&bars->k_full[stage], (j / kNSK) & 1, kWaitNs);
+                                  : __all_sync(0xffffffffu, mbar_wait_bounded(&bars->k_full[stage], (j / kNSK) & 1, kWaitNs));
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t kb = dk + uint64_t((stage * kTile) >> 4);
                     const uint32_t d = tbase + kColS + uint32_t(sb) * 128u;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {       // 16 head dims = 8 packed columns of Q
-                        const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
-                        mma_bf16_ts(d, tbase + kColQ + kk * 8, kb + koff, kIdS, kk > 0);
+                        for (int kk = 0; kk < kD / 16; ++kk) {   // 16 head dims = 8 packed columns of Q
+                            const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
+                            mma_bf16_ts(d, tbase + kColQ + kk * 8, kb + koff, kIdS, kk > 0);
+                        }
+                        if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
+                        else mma_commit_multicast(&bars->k_empty[stage], kMask);
+                        mma_commit(&bars->s_full[sb]);
                     }
-                    if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
-                    else mma_commit_multicast(&bars->k_empty[stage], kMask);
-                    mma_commit(&bars->s_full[sb]);
+                    __syncwarp();
                 }
             } else {
                 constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
@@ -330,22 +341,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // P_j sits in S_j's buffer: tokens 0-63 in columns [0, 32), tokens 64-127 in
                     // [64, 96) (each softmax warp overwrites only its own half of S)
                     const uint32_t pcol = tbase + kColS + uint32_t(sb) * 128u;
+                    if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {      // 16 tokens = 8 packed columns of P
-                        mma_bf16_ts(tbase + kColO, pcol + (kk >> 2) * 64 + (kk & 3) * 8, vb + uint64_t((kk * 2048) >> 4),
-                                    kIdO, (j > 0 || kk > 0));
+                        for (int kk = 0; kk < kBN / 16; ++kk) {  // 16 tokens = 8 packed columns of P
+                            mma_bf16_ts(tbase + kColO, pcol + (kk >> 2) * 64 + (kk & 3) * 8,
+                                        vb + uint64_t((kk * 2048) >> 4), kIdO, (j > 0 || kk > 0));
+                        }
+                        if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
+                        else mma_commit_multicast(&bars->v_empty[stage], kMask);
+                        mma_commit(&bars->s_free[sb]);
                     }
-                    if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
-                    else mma_commit_multicast(&bars->v_empty[stage], kMask);
-                    mma_commit(&bars->s_free[sb]);
+                    __syncwarp();
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
             }
             uint64_t* drain = &bars->drain[pv ? 1 : 0];
-            mma_commit(drain);                               // everything this thread issued has finished
+            if (elect_one()) mma_commit(drain);             // the pipe completes MMAs in issue order
+            __syncwarp();
             mbar_wait_bounded(drain, 0, kWaitNs);
         }
         __syncwarp();
