@@ -88,3 +88,16 @@ def depths(parents: np.ndarray) -> np.ndarray:
     for i in range(1, len(parents)):
         d[i] = d[parents[i]] + 1
     return d
+
+
+def random_root_path(parents: np.ndarray, rng: np.random.Generator, stop_prob: float = 0.25) -> list:
+    """A root-to-node walk through the tree (root excluded), in the form of an accept path:
+    at each node continue to a uniformly chosen child with probability 1 - stop_prob."""
+    kids = {}
+    for c in range(1, len(parents)):
+        kids.setdefault(int(parents[c]), []).append(c)
+    path, cur = [], 0
+    while kids.get(cur) and rng.random() >= stop_prob:
+        cur = int(rng.choice(kids[cur]))
+        path.append(cur)
+    return path
