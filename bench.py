@@ -262,6 +262,25 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K2
 
+    # ---- KV commit of the accepted paths (not part of the step above): timed on the resident
+    # pool with the accepted paths of the last step; it moves rows in place, so it runs last
+    new_lens = torch.empty_like(d["pl"])
+    ws_c = torch.empty(ts.commit_workspace_bytes(), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        ts.tree_kv_commit(d["k"], d["v"], d["pt"], d["pl"], path, alen, new_lens, workspace=ws_c, stream=stream)
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(K2):
+        ts.tree_kv_commit(d["k"], d["v"], d["pt"], d["pl"], path, alen, new_lens, workspace=ws_c, stream=stream)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    commit_ms = c0.elapsed_time(c1) / K2
+    if ts.read_status(ws_c):
+        raise RuntimeError("KV commit flagged an input error")
+    commit_bytes = int(alen.sum().item()) * w.num_kv_heads * w.head_dim * (2 if bf else 4) * 2 * 2
+
     # ---- report
     work = algorithmic_work(x)
     hbm, tf_burst, tf_sus, src = peaks()
@@ -304,6 +323,9 @@ def run_gpu(args):
         "e2e": {"value": round(world / (e2e_ms * 1e-3), 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
+        "kv_commit": {"ms": round(commit_ms, 4), "bytes": commit_bytes,
+                      "gbs": round(commit_bytes / (commit_ms * 1e-3) / 1e9, 1),
+                      "note": "tree_kv_commit of the step's accepted paths, timed apart from the step"},
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -27,7 +27,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 DTYPE_F32, DTYPE_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC = 0, 1, 2
 ACCEPT_AUTO, ACCEPT_ALL_ROWS, ACCEPT_PATH_ONLY = 0, 1, 2
-STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT", 32: "INTERNAL"}
+STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT", 32: "INTERNAL",
+               64: "BAD_PATH"}
 
 
 class AttnShape(ctypes.Structure):
@@ -56,6 +57,10 @@ _lib.tree_accept.restype = ctypes.c_int
 _lib.tree_accept_with_mode.argtypes = [_vp] * 5 + [ctypes.c_float] + [_vp] * 3 + [ctypes.c_int32] * 4 + \
     [_vp, ctypes.c_size_t, _vp]
 _lib.tree_accept_with_mode.restype = ctypes.c_int
+_lib.treespec_commit_workspace_bytes.argtypes = []
+_lib.treespec_commit_workspace_bytes.restype = ctypes.c_size_t
+_lib.tree_kv_commit.argtypes = [_vp] * 7 + [ctypes.POINTER(AttnShape), _vp, ctypes.c_size_t, _vp]
+_lib.tree_kv_commit.restype = ctypes.c_int
 _lib.treespec_read_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
 _lib.treespec_read_status.restype = ctypes.c_int
 _lib.treespec_error_string.argtypes = [ctypes.c_int]
@@ -219,6 +224,42 @@ def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms
         _ptr(accept_path), _ptr(accept_len), _ptr(bonus_token), B, N, V, int(mode),
         _ptr(workspace), workspace.numel(), _stream_handle(stream, dev)))
     return accept_path, accept_len, bonus_token
+
+
+def commit_workspace_bytes() -> int:
+    return int(_lib.treespec_commit_workspace_bytes())
+
+
+def tree_kv_commit(k_pages, v_pages, page_table, prefix_lens, accept_path, accept_len, new_prefix_lens=None, *,
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """Move the accepted path's K/V next to each prefix, in place; see include/treespec.h.
+
+    k_pages / v_pages [P][16][Hkv][D] (float32 or bfloat16), page_table [B][max_pages],
+    prefix_lens [B], accept_path [B][N], accept_len [B] (int32).  Returns new_prefix_lens
+    [B] int32 (prefix + 1 + accept_len, or -1 for a sequence left unchanged)."""
+    dev = k_pages.device
+    dt = k_pages.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise ValueError("k_pages must be float32 or bfloat16")
+    _need(k_pages, "k_pages", dt, dev)
+    _need(v_pages, "v_pages", dt, dev)
+    for name, t in (("page_table", page_table), ("prefix_lens", prefix_lens), ("accept_path", accept_path),
+                    ("accept_len", accept_len)):
+        _need(t, name, torch.int32, dev)
+    B, N = accept_path.shape
+    P, ps, Hkv, D = k_pages.shape
+    shape = AttnShape(B, N, Hkv, Hkv, D, ps, page_table.shape[1], P,
+                      DTYPE_BF16 if dt == torch.bfloat16 else DTYPE_F32, KERNEL_AUTO, 0)
+    if new_prefix_lens is None:
+        new_prefix_lens = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(new_prefix_lens, "new_prefix_lens", torch.int32, dev)
+    need = commit_workspace_bytes()
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(_lib.tree_kv_commit(_ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(prefix_lens), _ptr(accept_path),
+                               _ptr(accept_len), _ptr(new_prefix_lens), ctypes.byref(shape), _ptr(workspace),
+                               workspace.numel(), _stream_handle(stream, dev)))
+    return new_prefix_lens
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

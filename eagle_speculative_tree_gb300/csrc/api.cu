@@ -308,6 +308,48 @@ extern "C" int tree_accept(const float* target_logits, const int32_t* draft_toke
                                  TREESPEC_ACCEPT_AUTO, workspace, workspace_bytes, stream);
 }
 
+extern "C" size_t treespec_commit_workspace_bytes(void) { return kWsAlign; }
+
+extern "C" int tree_kv_commit(void* k_pages, void* v_pages, const int32_t* page_table,
+                              const int32_t* prefix_lens, const int32_t* accept_path,
+                              const int32_t* accept_len, int32_t* new_prefix_lens,
+                              const treespec_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                              treespec_stream_t stream) {
+    int rc = check_attn_shape(shape);
+    if (rc != TREESPEC_OK) return rc;
+    if (!k_pages || !v_pages || !page_table || !prefix_lens || !accept_path || !accept_len || !new_prefix_lens)
+        return TREESPEC_ERR_NULL_POINTER;
+    if (!aligned16(k_pages) || !aligned16(v_pages)) return TREESPEC_ERR_ALIGNMENT;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) ||
+        workspace_bytes < treespec_commit_workspace_bytes())
+        return TREESPEC_ERR_WORKSPACE;
+    rc = check_device();
+    if (rc != TREESPEC_OK) return rc;
+    const treespec_attn_shape& s = *shape;
+    CommitParams p{};
+    p.k = k_pages;
+    p.v = v_pages;
+    p.page_table = page_table;
+    p.prefix_lens = prefix_lens;
+    p.path = accept_path;
+    p.len = accept_len;
+    p.new_lens = new_prefix_lens;
+    p.status = static_cast<uint32_t*>(workspace);
+    p.B = s.batch;
+    p.N = s.num_nodes;
+    p.Hkv = s.num_kv_heads;
+    p.D = s.head_dim;
+    p.ps = s.page_size;
+    p.max_pages = s.max_pages_per_seq;
+    p.num_pool_pages = s.num_pool_pages;
+    p.elem = s.dtype == TREESPEC_DTYPE_BF16 ? 2 : 4;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (launch_kv_commit(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches++;
+    return TREESPEC_OK;
+}
+
 extern "C" int treespec_read_status(const void* workspace, uint32_t* status, treespec_stream_t stream) {
     if (!workspace || !status) return TREESPEC_ERR_NULL_POINTER;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -106,6 +106,20 @@ bool attn_tc_supported(int dtype, int D);
 int attn_tc_cluster_size(int row_blocks);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptParams& p, int mode, cudaStream_t s, int* kernels);
+
+// KV commit (tree_kv_commit)
+struct CommitParams {
+    void* k;
+    void* v;
+    const int32_t* page_table;
+    const int32_t* prefix_lens;
+    const int32_t* path;
+    const int32_t* len;
+    int32_t* new_lens;
+    uint32_t* status;
+    int B, N, Hkv, D, ps, max_pages, num_pool_pages, elem;   // elem: bytes per element
+};
+cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s);
 size_t attn_simt_smem_bytes(int dtype, int D, int R_block);
 
 }  // namespace treespec

@@ -80,6 +80,7 @@ enum treespec_status_bits {
     TREESPEC_STATUS_BAD_TOKEN = 1u << 3,   /* a draft token outside [0, vocab) */
     TREESPEC_STATUS_TIMEOUT = 1u << 4,     /* a bounded wait inside a kernel ran out */
     TREESPEC_STATUS_INTERNAL = 1u << 5,    /* a launch-configuration invariant failed (work skipped) */
+    TREESPEC_STATUS_BAD_PATH = 1u << 6,    /* tree_kv_commit: accept_len or accept_path out of range */
 };
 
 /* ------------------------------------------------------------------ tree attention */
@@ -221,6 +222,42 @@ int tree_accept_with_mode(const float *target_logits, const int32_t *draft_token
                           int32_t *accept_path, int32_t *accept_len, int32_t *bonus_token,
                           int32_t batch, int32_t num_nodes, int32_t vocab, int32_t mode,
                           void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
+/* ----------------------------------------------------------------------- KV commit */
+
+/* Workspace bytes tree_kv_commit needs (its status word). */
+size_t treespec_commit_workspace_bytes(void);
+
+/*
+ * tree_kv_commit -- keep the accepted path's K/V, drop the rejected branches
+ * ("Tech Radar: SGLang EAGLE-2", section 2: after verification the target retains the
+ * accepted path's KV and discards the rejected branches; "EAGLE-2 & Lookahead
+ * Decoding", section 6, paged tree KV-cache allocation: the positions of rejected
+ * candidates go back to the pool).
+ *
+ * As tree_attn_verify lays a tree out, node n of sequence b sits at logical position
+ * S + n (S = prefix_lens[b]) and node 0 is the root.  For k < accept_len[b] the K and V
+ * rows (all kv heads) of node accept_path[b][k] are copied to logical position
+ * S + 1 + k, in place in the page pool, and new_prefix_lens[b] = S + 1 + accept_len[b]:
+ * the sequence then ends with the root and its accepted descendants, and the positions
+ * after it are free for the next tree.  Every source row is read before any destination
+ * row is written, so overlapping positions are safe.
+ *   k_pages, v_pages  [P][16][Hkv][D] in shape->dtype, modified in place
+ *   page_table [B][max_pages], prefix_lens [B]   int32, as given to tree_attn_verify
+ *   accept_path [B][N], accept_len [B]           int32, as returned by tree_accept
+ *   new_prefix_lens [B]                          int32 out (a separate buffer)
+ *   shape: batch, num_nodes, num_kv_heads, head_dim, page_size, max_pages_per_seq,
+ *          num_pool_pages and dtype are used; num_q_heads, kernel, num_splits are not.
+ * A sequence whose prefix length is invalid (BAD_LENGTH), whose accept_len is outside
+ * [0, N-1] or whose path does not increase strictly within [1, N) (BAD_PATH), or whose
+ * pages touched are outside the pool (BAD_PAGE) is left unchanged and gets
+ * new_prefix_lens[b] = -1; the bit goes to the workspace status word.
+ */
+int tree_kv_commit(void *k_pages, void *v_pages, const int32_t *page_table,
+                   const int32_t *prefix_lens, const int32_t *accept_path,
+                   const int32_t *accept_len, int32_t *new_prefix_lens,
+                   const treespec_attn_shape *shape,
+                   void *workspace, size_t workspace_bytes, treespec_stream_t stream);
 
 /* ------------------------------------------------------------------------- helpers */
 
