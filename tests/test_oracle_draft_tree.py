@@ -1,0 +1,125 @@
+"""Pins of oracle.draft_tree (beam expansion and rerank; CPU only)."""
+import inspect
+
+import numpy as np
+import pytest
+
+from oracle import draft_tree as odt
+
+
+def log_rows(rng, shape, ties=False):
+    p = rng.dirichlet(np.ones(shape[-1]) * 0.5, size=shape[:-1])
+    lp = np.log(np.maximum(p, 1e-30)).astype(np.float32)
+    if ties:                                            # repeated values exercise the tie rules
+        lp = np.round(lp * 2) / 2
+    return lp
+
+
+def run_steps(lp_steps, k):
+    B = lp_steps[0].shape[0]
+    M = 1 + len(lp_steps) * k
+    par = np.zeros((B, M), np.int32)
+    tok = np.zeros((B, M), np.int32)
+    sc = np.zeros((B, M), np.float32)
+    for s, lp in enumerate(lp_steps):
+        odt.draft_step(lp, par, tok, sc, s, k)
+    return par, tok, sc
+
+
+@pytest.mark.parametrize("seed,ties", [(0, False), (1, True), (2, True), (3, False)])
+def test_step_equals_top_k_over_all_frontier_token_pairs(seed, ties):
+    # brute force: no per-node preselection -- rank every (frontier f, token v) pair by
+    # (score desc, f, v) and take k; equal to the two-stage rule because a pair in the
+    # global top k has at most k-1 better pairs, so it is within its own node's top k
+    rng = np.random.default_rng(seed)
+    k, V = 3, 7
+    lp0 = log_rows(rng, (2, 1, V), ties)
+    lp1 = log_rows(rng, (2, k, V), ties)
+    par, tok, sc = run_steps([lp0, lp1], k)
+    for b in range(2):
+        frontier = [1, 2, 3]
+        pairs = [(np.float32(sc[b, n] + lp1[b, f, v]), f, v) for f, n in enumerate(frontier) for v in range(V)]
+        best = sorted(pairs, key=lambda t: (-float(t[0]), t[1], t[2]))[:k]
+        assert [(int(par[b, 4 + r]), int(tok[b, 4 + r])) for r in range(k)] == \
+            [(frontier[f], v) for _s, f, v in best]
+        assert np.array_equal(sc[b, 4:], np.array([s for s, _f, _v in best], np.float32))
+
+
+def test_topk_one_is_the_greedy_chain():
+    rng = np.random.default_rng(7)
+    steps = [log_rows(rng, (3, 1, 11)) for _ in range(5)]
+    par, tok, sc = run_steps(steps, 1)
+    for b in range(3):
+        assert par[b].tolist() == [-1, 0, 1, 2, 3, 4]
+        assert tok[b, 1:].tolist() == [int(np.argmax(s[b, 0])) for s in steps]
+        assert np.isclose(sc[b, -1], sum(float(np.max(s[b, 0])) for s in steps), rtol=1e-5)
+
+
+def test_rerank_hand_example():
+    # root, a(-0.1, root), b(-0.5, root), c(-0.3, a), d(-2.0, b), e(-0.3, c): keep 4 of 5
+    # by score: a(-0.1), c(-0.3, index 3), e(-0.3, index 5), b(-0.5); drop d.  Numbered by
+    # original index: a->1, b->2, c->3, e->4; parents a:0, b:0, c:1 (a), e:3 (c).
+    par = np.array([[-1, 0, 0, 1, 2, 3]], np.int32)
+    tok = np.array([[-1, 10, 20, 30, 40, 50]], np.int32)
+    sc = np.array([[0, -0.1, -0.5, -0.3, -2.0, -0.3]], np.float32)
+    parents, tokens, st = odt.rerank(par, tok, sc, num_nodes=5)
+    assert st == 0
+    assert parents.tolist() == [[-1, 0, 0, 1, 3]]
+    assert tokens.tolist() == [[-1, 10, 20, 30, 50]]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_built_trees_are_ancestor_closed_and_scores_are_path_sums(seed):
+    rng = np.random.default_rng(seed)
+    k, steps, N, V = 4, 5, 12, 9
+    lps = [log_rows(rng, (2, 1 if s == 0 else k, V)) for s in range(steps)]
+    par, tok, sc = run_steps(lps, k)
+    parents, tokens, st = odt.rerank(par, tok, sc, N)
+    assert st == 0
+    for b in range(2):
+        assert parents[b, 0] == -1 and all(0 <= parents[b, i] < i for i in range(1, N))
+        # every node's score is the float32 running sum of the log-probs along its path
+        for i in range(1, par.shape[1]):
+            chain, n = [], i
+            while n > 0:
+                chain.append(n)
+                n = int(par[b, n])
+            s = np.float32(0)
+            for n in reversed(chain):
+                depth = (n - 1) // k
+                row = 0 if depth == 0 else (int(par[b, n]) - 1 - (depth - 1) * k)
+                s = np.float32(s + lps[depth][b, row, tok[b, n]])
+            assert s == sc[b, i]
+
+
+def test_rerank_keeping_everything_is_the_identity():
+    rng = np.random.default_rng(11)
+    par, tok, sc = run_steps([log_rows(rng, (1, 1, 6)), log_rows(rng, (1, 2, 6))], 2)
+    parents, tokens, st = odt.rerank(par, tok, sc, num_nodes=5)
+    assert st == 0 and parents[0].tolist() == par[0].tolist() and tokens[0].tolist() == tok[0].tolist()
+
+
+def test_positive_logprobs_can_orphan_and_are_flagged():
+    par = np.array([[-1, 0, 1]], np.int32)
+    tok = np.array([[-1, 5, 6]], np.int32)
+    sc = np.array([[0, -1.0, 2.0]], np.float32)       # the child outscores its parent
+    parents, _t, st = odt.rerank(par, tok, sc, num_nodes=2)
+    assert st & odt.BAD_PARENT and parents.tolist() == [[-1, 0]]
+
+
+def test_planted_reversed_ranking_fails_the_brute_force():
+    src = inspect.getsource(odt.draft_step).replace("cands.sort(key=lambda c: (-float(c[0]), c[1]))",
+                                                    "cands.sort(key=lambda c: (float(c[0]), c[1]))")
+    ns = {"np": np}
+    exec(src, ns)
+    rng = np.random.default_rng(0)
+    lp0 = log_rows(rng, (1, 1, 7))
+    lp1 = log_rows(rng, (1, 3, 7))
+    par = np.zeros((1, 7), np.int32)
+    tok = np.zeros((1, 7), np.int32)
+    sc = np.zeros((1, 7), np.float32)
+    odt.draft_step(lp0, par, tok, sc, 0, 3)
+    ns["draft_step"](lp1, par, tok, sc, 1, 3)
+    pairs = [(np.float32(sc[0, n] + lp1[0, f, v]), f, v) for f, n in enumerate([1, 2, 3]) for v in range(7)]
+    best = sorted(pairs, key=lambda t: (-float(t[0]), t[1], t[2]))[:3]
+    assert [(int(par[0, 4 + r]), int(tok[0, 4 + r])) for r in range(3)] != [(1 + f, v) for _s, f, v in best]
