@@ -10,16 +10,19 @@ EAGLE decoding): each draft step branches every expanded node into its top
 the top `speculative_num_draft_tokens` nodes as the draft tree.
 
 Readings where the pages are silent (the CUDA entry points follow the same ones):
-  * node 0 is the root (score 0); step s (0-based) adds nodes 1 + s*k .. 1 + s*k + k - 1;
-    the frontier of step 0 is the root, of step s > 0 the k nodes step s - 1 added;
-  * a frontier node's children are its top-k tokens by log-probability, ties to the
-    lower token id; of the F*k candidates (frontier f, rank r) the k with the highest
-    score are kept, ties to the lower candidate index f*k + r, in descending score order;
+  * node 0 is the root (score 0).  Step s (0-based) expands a frontier of F nodes (the
+    root at step 0, F = 1; the k best candidates of step s - 1 after that, F = k): each
+    frontier node's children are its top-k tokens by log-probability, ties to the lower
+    token id, and every one of the F*k candidates (frontier row f, rank r; candidate
+    index f*k + r) becomes a node, in candidate order, from node base(s) = 1 at s = 0 and
+    1 + k + (s - 1)*k*k after that.  The next frontier is the k candidates with the
+    highest score, ties to the lower candidate index, best first;
   * scores are float32 sums (parent score + log-probability), the precision the kernel
     decides in, so both sides rank identically;
   * the rerank keeps the root and the N - 1 non-root nodes with the highest score, ties
     to the lower node index, numbered in increasing original index (a topological order,
-    since a node's parent was added before it).  A kept node whose parent was dropped
+    since a node's parent was added before it).  All scored candidates are eligible, so
+    a tree may be larger than steps * k nodes.  A kept node whose parent was dropped
     (only possible with positive log-probabilities) is attached to the root and flagged.
 """
 from __future__ import annotations
@@ -29,30 +32,43 @@ import numpy as np
 BAD_PARENT = 1
 
 
-def draft_step(logprobs: np.ndarray, node_parent: np.ndarray, node_token: np.ndarray, node_score: np.ndarray,
-               step: int, topk: int) -> None:
+def step_base(step: int, topk: int) -> int:
+    """First node index of a step's candidates."""
+    return 1 if step == 0 else 1 + topk + (step - 1) * topk * topk
+
+
+def num_nodes_after(steps: int, topk: int) -> int:
+    return step_base(steps, topk)
+
+
+def draft_step(logprobs: np.ndarray, frontier: np.ndarray, node_parent: np.ndarray, node_token: np.ndarray,
+               node_score: np.ndarray, step: int, topk: int) -> np.ndarray:
     """One expansion step, in place on the node arrays [B][M].  logprobs [B][F][V] float32,
-    one row per frontier node (F = 1 at step 0, else topk)."""
+    one row per frontier node in the order of `frontier` [B][F] (ignored at step 0).
+    Returns the next frontier [B][k] (node indices, best first)."""
     B, F, V = logprobs.shape
     k = topk
+    base = step_base(step, k)
+    nxt = np.zeros((B, k), dtype=np.int32)
     for b in range(B):
         if step == 0:
             node_parent[b, 0], node_token[b, 0], node_score[b, 0] = -1, -1, np.float32(0.0)
-            frontier = [0]
+            front = [0]
         else:
-            frontier = list(range(1 + (step - 1) * k, 1 + step * k))
-        assert len(frontier) == F
-        cands = []                                           # (score, candidate index, parent node, token)
-        for f, node in enumerate(frontier):
+            front = [int(x) for x in frontier[b]]
+        assert len(front) == F
+        cands = []                                           # (score, candidate index)
+        for f, node in enumerate(front):
             row = logprobs[b, f].astype(np.float32)
-            order = sorted(range(V), key=lambda v: (-float(row[v]), v))[:k]
+            order = [int(v) for v in np.lexsort((np.arange(V), -row.astype(np.float64)))[:k]]   # value desc, id asc
             for r, tok in enumerate(order):
+                c = f * k + r
                 score = np.float32(np.float32(node_score[b, node]) + row[tok])
-                cands.append((score, f * k + r, node, tok))
-        cands.sort(key=lambda c: (-float(c[0]), c[1]))
-        for r, (score, _ci, node, tok) in enumerate(cands[:k]):
-            i = 1 + step * k + r
-            node_parent[b, i], node_token[b, i], node_score[b, i] = node, tok, score
+                node_parent[b, base + c], node_token[b, base + c], node_score[b, base + c] = node, tok, score
+                cands.append((score, c))
+        cands.sort(key=lambda t: (-float(t[0]), t[1]))
+        nxt[b] = [base + c for _s, c in cands[:k]]
+    return nxt
 
 
 def rerank(node_parent: np.ndarray, node_token: np.ndarray, node_score: np.ndarray, num_nodes: int):

@@ -17,13 +17,16 @@ def log_rows(rng, shape, ties=False):
 
 def run_steps(lp_steps, k):
     B = lp_steps[0].shape[0]
-    M = 1 + len(lp_steps) * k
+    M = odt.num_nodes_after(len(lp_steps), k)
     par = np.zeros((B, M), np.int32)
     tok = np.zeros((B, M), np.int32)
     sc = np.zeros((B, M), np.float32)
+    front = np.zeros((B, 1), np.int32)
+    fronts = []
     for s, lp in enumerate(lp_steps):
-        odt.draft_step(lp, par, tok, sc, s, k)
-    return par, tok, sc
+        front = odt.draft_step(lp, front, par, tok, sc, s, k)
+        fronts.append(front)
+    return par, tok, sc, fronts
 
 
 @pytest.mark.parametrize("seed,ties", [(0, False), (1, True), (2, True), (3, False)])
@@ -35,20 +38,20 @@ def test_step_equals_top_k_over_all_frontier_token_pairs(seed, ties):
     k, V = 3, 7
     lp0 = log_rows(rng, (2, 1, V), ties)
     lp1 = log_rows(rng, (2, k, V), ties)
-    par, tok, sc = run_steps([lp0, lp1], k)
+    par, tok, sc, fronts = run_steps([lp0, lp1], k)
     for b in range(2):
-        frontier = [1, 2, 3]
+        frontier = fronts[0][b].tolist()                     # step 1 expanded these, in this order
+        assert sorted(frontier) == [1, 2, 3]                 # step 0: the root's k children, all kept
         pairs = [(np.float32(sc[b, n] + lp1[b, f, v]), f, v) for f, n in enumerate(frontier) for v in range(V)]
         best = sorted(pairs, key=lambda t: (-float(t[0]), t[1], t[2]))[:k]
-        assert [(int(par[b, 4 + r]), int(tok[b, 4 + r])) for r in range(k)] == \
-            [(frontier[f], v) for _s, f, v in best]
-        assert np.array_equal(sc[b, 4:], np.array([s for s, _f, _v in best], np.float32))
+        got = [(int(par[b, n]), int(tok[b, n]), sc[b, n]) for n in fronts[1][b]]
+        assert got == [(frontier[f], v, s) for s, f, v in best]
 
 
 def test_topk_one_is_the_greedy_chain():
     rng = np.random.default_rng(7)
     steps = [log_rows(rng, (3, 1, 11)) for _ in range(5)]
-    par, tok, sc = run_steps(steps, 1)
+    par, tok, sc, _f = run_steps(steps, 1)
     for b in range(3):
         assert par[b].tolist() == [-1, 0, 1, 2, 3, 4]
         assert tok[b, 1:].tolist() == [int(np.argmax(s[b, 0])) for s in steps]
@@ -71,31 +74,33 @@ def test_rerank_hand_example():
 @pytest.mark.parametrize("seed", range(5))
 def test_built_trees_are_ancestor_closed_and_scores_are_path_sums(seed):
     rng = np.random.default_rng(seed)
-    k, steps, N, V = 4, 5, 12, 9
+    k, steps, N, V = 4, 5, 40, 9
     lps = [log_rows(rng, (2, 1 if s == 0 else k, V)) for s in range(steps)]
-    par, tok, sc = run_steps(lps, k)
+    par, tok, sc, fronts = run_steps(lps, k)
+    assert par.shape[1] == 1 + 4 + 4 * 16                  # every scored candidate is a node
     parents, tokens, st = odt.rerank(par, tok, sc, N)
     assert st == 0
     for b in range(2):
         assert parents[b, 0] == -1 and all(0 <= parents[b, i] < i for i in range(1, N))
-        # every node's score is the float32 running sum of the log-probs along its path
+        # every node's score is the float32 running sum of the log-probs along its path;
+        # a node of step s > 0 came from the row of its parent in step s - 1's frontier
         for i in range(1, par.shape[1]):
             chain, n = [], i
             while n > 0:
                 chain.append(n)
                 n = int(par[b, n])
             s = np.float32(0)
-            for n in reversed(chain):
-                depth = (n - 1) // k
-                row = 0 if depth == 0 else (int(par[b, n]) - 1 - (depth - 1) * k)
+            for depth, n in enumerate(reversed(chain)):
+                row = 0 if depth == 0 else fronts[depth - 1][b].tolist().index(int(par[b, n]))
                 s = np.float32(s + lps[depth][b, row, tok[b, n]])
             assert s == sc[b, i]
 
 
 def test_rerank_keeping_everything_is_the_identity():
     rng = np.random.default_rng(11)
-    par, tok, sc = run_steps([log_rows(rng, (1, 1, 6)), log_rows(rng, (1, 2, 6))], 2)
-    parents, tokens, st = odt.rerank(par, tok, sc, num_nodes=5)
+    par, tok, sc, _f = run_steps([log_rows(rng, (1, 1, 6)), log_rows(rng, (1, 2, 6))], 2)
+    assert par.shape[1] == 7
+    parents, tokens, st = odt.rerank(par, tok, sc, num_nodes=7)
     assert st == 0 and parents[0].tolist() == par[0].tolist() and tokens[0].tolist() == tok[0].tolist()
 
 
@@ -108,18 +113,20 @@ def test_positive_logprobs_can_orphan_and_are_flagged():
 
 
 def test_planted_reversed_ranking_fails_the_brute_force():
-    src = inspect.getsource(odt.draft_step).replace("cands.sort(key=lambda c: (-float(c[0]), c[1]))",
-                                                    "cands.sort(key=lambda c: (float(c[0]), c[1]))")
-    ns = {"np": np}
+    src = inspect.getsource(odt.draft_step).replace("cands.sort(key=lambda t: (-float(t[0]), t[1]))",
+                                                    "cands.sort(key=lambda t: (float(t[0]), t[1]))")
+    ns = {"np": np, "step_base": odt.step_base}
     exec(src, ns)
     rng = np.random.default_rng(0)
     lp0 = log_rows(rng, (1, 1, 7))
     lp1 = log_rows(rng, (1, 3, 7))
-    par = np.zeros((1, 7), np.int32)
-    tok = np.zeros((1, 7), np.int32)
-    sc = np.zeros((1, 7), np.float32)
-    odt.draft_step(lp0, par, tok, sc, 0, 3)
-    ns["draft_step"](lp1, par, tok, sc, 1, 3)
-    pairs = [(np.float32(sc[0, n] + lp1[0, f, v]), f, v) for f, n in enumerate([1, 2, 3]) for v in range(7)]
+    M = odt.num_nodes_after(2, 3)
+    par = np.zeros((1, M), np.int32)
+    tok = np.zeros((1, M), np.int32)
+    sc = np.zeros((1, M), np.float32)
+    f0 = odt.draft_step(lp0, np.zeros((1, 1), np.int32), par, tok, sc, 0, 3)
+    f1 = ns["draft_step"](lp1, f0, par, tok, sc, 1, 3)
+    frontier = f0[0].tolist()
+    pairs = [(np.float32(sc[0, n] + lp1[0, f, v]), f, v) for f, n in enumerate(frontier) for v in range(7)]
     best = sorted(pairs, key=lambda t: (-float(t[0]), t[1], t[2]))[:3]
-    assert [(int(par[0, 4 + r]), int(tok[0, 4 + r])) for r in range(3)] != [(1 + f, v) for _s, f, v in best]
+    assert [(int(par[0, n]), int(tok[0, n])) for n in f1[0]] != [(frontier[f], v) for _s, f, v in best]
