@@ -281,6 +281,46 @@ def run_gpu(args):
         raise RuntimeError("KV commit flagged an input error")
     commit_bytes = int(alen.sum().item()) * w.num_kv_heads * w.head_dim * (2 if bf else 4) * 2 * 2
 
+    # ---- draft-tree build for the next step (not part of the step above): the workload's
+    # num_steps steps of top-k expansion over the vocabulary, then the rerank to N nodes
+    from gen import draft as gdraft
+    k_d, steps_d = w.topk, w.num_steps
+    M_d = 1 + k_d + (steps_d - 1) * k_d * k_d
+    lp0 = torch.from_numpy(gdraft.draft_logprobs(1000 + w.cfg_id, w.batch, 1, w.vocab)).to(dev)
+    lpk = torch.from_numpy(gdraft.draft_logprobs(2000 + w.cfg_id, w.batch, k_d, w.vocab)).to(dev)
+    npar = torch.zeros((w.batch, M_d), dtype=torch.int32, device=dev)
+    ntok = torch.zeros_like(npar)
+    nsc = torch.zeros((w.batch, M_d), dtype=torch.float32, device=dev)
+    fronts = [torch.empty((w.batch, k_d), dtype=torch.int32, device=dev) for _ in range(2)]
+    ws_d = torch.empty(ts.draft_workspace_bytes(w.batch, k_d, k_d), dtype=torch.uint8, device=dev)
+    ws_r = torch.empty(256, dtype=torch.uint8, device=dev)
+    tp = torch.empty((w.batch, w.num_nodes), dtype=torch.int32, device=dev)
+    tt = torch.empty_like(tp)
+
+    def build_tree():
+        front = None
+        for s_ in range(steps_d):
+            out = fronts[s_ & 1]
+            ts.tree_draft_step(lp0 if s_ == 0 else lpk, s_, k_d, front, npar, ntok, nsc, out, workspace=ws_d,
+                               stream=stream)
+            front = out
+        ts.tree_rerank(npar, ntok, nsc, w.num_nodes, tp, tt, workspace=ws_r, stream=stream)
+
+    for _ in range(3):
+        build_tree()
+    torch.cuda.synchronize()
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(K2):
+        build_tree()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    draft_ms = d0.elapsed_time(d1) / K2
+    if ts.read_status(ws_d) or ts.read_status(ws_r):
+        raise RuntimeError("draft-tree build flagged an input error")
+    draft_bytes = (w.batch * w.vocab * 4) * (1 + (steps_d - 1) * k_d)
+
     # ---- report
     work = algorithmic_work(x)
     hbm, tf_burst, tf_sus, src = peaks()
@@ -326,6 +366,9 @@ def run_gpu(args):
         "kv_commit": {"ms": round(commit_ms, 4), "bytes": commit_bytes,
                       "gbs": round(commit_bytes / (commit_ms * 1e-3) / 1e9, 1),
                       "note": "tree_kv_commit of the step's accepted paths, timed apart from the step"},
+        "draft_tree": {"ms": round(draft_ms, 4), "bytes": draft_bytes,
+                       "gbs": round(draft_bytes / (draft_ms * 1e-3) / 1e9, 1), "steps": steps_d, "topk": k_d,
+                       "note": "tree_draft_step x steps + tree_rerank for the next tree, timed apart from the step"},
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

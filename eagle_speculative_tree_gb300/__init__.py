@@ -61,6 +61,12 @@ _lib.treespec_commit_workspace_bytes.argtypes = []
 _lib.treespec_commit_workspace_bytes.restype = ctypes.c_size_t
 _lib.tree_kv_commit.argtypes = [_vp] * 7 + [ctypes.POINTER(AttnShape), _vp, ctypes.c_size_t, _vp]
 _lib.tree_kv_commit.restype = ctypes.c_int
+_lib.treespec_draft_workspace_bytes.argtypes = [ctypes.c_int32] * 3
+_lib.treespec_draft_workspace_bytes.restype = ctypes.c_size_t
+_lib.tree_draft_step.argtypes = [_vp] + [ctypes.c_int32] * 5 + [_vp] * 4 + [ctypes.c_int32, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.tree_draft_step.restype = ctypes.c_int
+_lib.tree_rerank.argtypes = [_vp] * 3 + [ctypes.c_int32] * 3 + [_vp] * 3 + [ctypes.c_size_t, _vp]
+_lib.tree_rerank.restype = ctypes.c_int
 _lib.treespec_read_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
 _lib.treespec_read_status.restype = ctypes.c_int
 _lib.treespec_error_string.argtypes = [ctypes.c_int]
@@ -260,6 +266,62 @@ def tree_kv_commit(k_pages, v_pages, page_table, prefix_lens, accept_path, accep
                                _ptr(accept_len), _ptr(new_prefix_lens), ctypes.byref(shape), _ptr(workspace),
                                workspace.numel(), _stream_handle(stream, dev)))
     return new_prefix_lens
+
+
+def draft_workspace_bytes(batch: int, frontier: int, topk: int) -> int:
+    n = _lib.treespec_draft_workspace_bytes(batch, frontier, topk)
+    if n == 0:
+        raise ValueError("unsupported draft-step sizes")
+    return int(n)
+
+
+def tree_draft_step(logprobs, step: int, topk: int, frontier_in, node_parent, node_token, node_score,
+                    frontier_out=None, *, workspace: Optional[torch.Tensor] = None, stream=None):
+    """One beam-expansion step of the draft tree, in place on the node arrays; see
+    include/treespec.h.  logprobs [B][F][V] float32 (F = 1 at step 0, else topk);
+    frontier_in [B][F] int32 (the previous step's result; None at step 0); node_parent /
+    node_token [B][M] int32, node_score [B][M] float32.  Returns (frontier_out [B][topk],
+    workspace)."""
+    dev = logprobs.device
+    _need(logprobs, "logprobs", torch.float32, dev)
+    _need(node_parent, "node_parent", torch.int32, dev)
+    _need(node_token, "node_token", torch.int32, dev)
+    _need(node_score, "node_score", torch.float32, dev)
+    if frontier_in is not None:
+        _need(frontier_in, "frontier_in", torch.int32, dev)
+    B, F, V = logprobs.shape
+    M = node_parent.shape[1]
+    if frontier_out is None:
+        frontier_out = torch.empty((B, topk), dtype=torch.int32, device=dev)
+    _need(frontier_out, "frontier_out", torch.int32, dev)
+    need = draft_workspace_bytes(B, F, topk)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(_lib.tree_draft_step(_ptr(logprobs), B, F, V, topk, step, _ptr(frontier_in), _ptr(node_parent),
+                                _ptr(node_token), _ptr(node_score), M, _ptr(frontier_out), _ptr(workspace),
+                                workspace.numel(), _stream_handle(stream, dev)))
+    return frontier_out, workspace
+
+
+def tree_rerank(node_parent, node_token, node_score, num_nodes: int, tree_parents=None, draft_tokens=None, *,
+                workspace: Optional[torch.Tensor] = None, stream=None):
+    """Keep the root and the num_nodes - 1 best nodes; returns (tree_parents, draft_tokens)
+    [B][num_nodes] int32.  See include/treespec.h."""
+    dev = node_parent.device
+    _need(node_parent, "node_parent", torch.int32, dev)
+    _need(node_token, "node_token", torch.int32, dev)
+    _need(node_score, "node_score", torch.float32, dev)
+    B, M = node_parent.shape
+    if tree_parents is None:
+        tree_parents = torch.empty((B, num_nodes), dtype=torch.int32, device=dev)
+    if draft_tokens is None:
+        draft_tokens = torch.empty((B, num_nodes), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=dev)
+    _check(_lib.tree_rerank(_ptr(node_parent), _ptr(node_token), _ptr(node_score), B, M, num_nodes,
+                            _ptr(tree_parents), _ptr(draft_tokens), _ptr(workspace), workspace.numel(),
+                            _stream_handle(stream, dev)))
+    return tree_parents, draft_tokens
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

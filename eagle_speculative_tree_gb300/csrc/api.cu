@@ -350,6 +350,85 @@ extern "C" int tree_kv_commit(void* k_pages, void* v_pages, const int32_t* page_
     return TREESPEC_OK;
 }
 
+extern "C" size_t treespec_draft_workspace_bytes(int32_t batch, int32_t frontier, int32_t topk) {
+    if (batch < 1 || batch > 65535 || frontier < 1 || frontier > kMaxFrontier || topk < 1 || topk > kMaxTopk)
+        return 0;
+    const size_t per = size_t(batch) * frontier * topk;
+    return kWsAlign + align_up(per * 4, kWsAlign) * 2;
+}
+
+extern "C" int tree_draft_step(const float* logprobs, int32_t batch, int32_t frontier, int32_t vocab,
+                               int32_t topk, int32_t step, const int32_t* frontier_in, int32_t* node_parent,
+                               int32_t* node_token, float* node_score, int32_t max_nodes, int32_t* frontier_out,
+                               void* workspace, size_t workspace_bytes, treespec_stream_t stream) {
+    if (batch < 1 || batch > 65535 || topk < 1 || topk > kMaxTopk || step < 0) return TREESPEC_ERR_SHAPE;
+    if (frontier != (step == 0 ? 1 : topk)) return TREESPEC_ERR_SHAPE;
+    if (vocab < topk || vocab > (1 << 30)) return TREESPEC_ERR_SHAPE;
+    const long long base = step == 0 ? 1 : 1 + topk + (long long)(step - 1) * topk * topk;
+    if (max_nodes > kMaxDraftNodes || base + (long long)frontier * topk > max_nodes) return TREESPEC_ERR_SHAPE;
+    if ((long long)batch * frontier * vocab > (1ll << 40)) return TREESPEC_ERR_SHAPE;
+    if (!logprobs || !node_parent || !node_token || !node_score || !frontier_out || (step > 0 && !frontier_in))
+        return TREESPEC_ERR_NULL_POINTER;
+    if (vocab % 4 == 0 && !aligned16(logprobs)) return TREESPEC_ERR_ALIGNMENT;
+    const size_t need = treespec_draft_workspace_bytes(batch, frontier, topk);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) || workspace_bytes < need)
+        return TREESPEC_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc != TREESPEC_OK) return rc;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const size_t per = size_t(batch) * frontier * topk;
+    DraftParams p{};
+    p.logprobs = logprobs;
+    p.frontier_in = frontier_in;
+    p.frontier_out = frontier_out;
+    p.node_parent = node_parent;
+    p.node_token = node_token;
+    p.node_score = node_score;
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.tk_tok = reinterpret_cast<int32_t*>(ws + kWsAlign);
+    p.tk_lp = reinterpret_cast<float*>(ws + kWsAlign + align_up(per * 4, kWsAlign));
+    p.B = batch;
+    p.F = frontier;
+    p.V = vocab;
+    p.k = topk;
+    p.step = step;
+    p.M = max_nodes;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (launch_draft_step(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches += 2;
+    return TREESPEC_OK;
+}
+
+extern "C" int tree_rerank(const int32_t* node_parent, const int32_t* node_token, const float* node_score,
+                           int32_t batch, int32_t max_nodes, int32_t num_nodes, int32_t* tree_parents,
+                           int32_t* draft_tokens, void* workspace, size_t workspace_bytes,
+                           treespec_stream_t stream) {
+    if (batch < 1 || batch > 65535 || max_nodes < 1 || max_nodes > kMaxDraftNodes) return TREESPEC_ERR_SHAPE;
+    if (num_nodes < 1 || num_nodes > kMaxNodes || num_nodes > max_nodes) return TREESPEC_ERR_SHAPE;
+    if (!node_parent || !node_token || !node_score || !tree_parents || !draft_tokens)
+        return TREESPEC_ERR_NULL_POINTER;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) || workspace_bytes < kWsAlign)
+        return TREESPEC_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc != TREESPEC_OK) return rc;
+    RerankParams p{};
+    p.node_parent = node_parent;
+    p.node_token = node_token;
+    p.node_score = node_score;
+    p.parents = tree_parents;
+    p.tokens = draft_tokens;
+    p.status = static_cast<uint32_t*>(workspace);
+    p.B = batch;
+    p.M = max_nodes;
+    p.N = num_nodes;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (launch_rerank(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    g_launches++;
+    return TREESPEC_OK;
+}
+
 extern "C" int treespec_read_status(const void* workspace, uint32_t* status, treespec_stream_t stream) {
     if (!workspace || !status) return TREESPEC_ERR_NULL_POINTER;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -120,6 +120,34 @@ struct CommitParams {
     int B, N, Hkv, D, ps, max_pages, num_pool_pages, elem;   // elem: bytes per element
 };
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s);
+
+// Draft-tree construction (tree_draft_step, tree_rerank)
+constexpr int kMaxTopk = 16;          // branching per step
+constexpr int kMaxFrontier = 16;      // frontier rows per step (1 or topk)
+constexpr int kMaxDraftNodes = 1024;  // node arrays of a sequence (root + steps * topk)
+struct DraftParams {
+    const float* logprobs;            // [B][F][V]
+    const int32_t* frontier_in;       // [B][F] node ids (unused at step 0)
+    int32_t* frontier_out;            // [B][k]
+    int32_t* node_parent;             // [B][M]
+    int32_t* node_token;
+    float* node_score;
+    int32_t* tk_tok;                  // workspace: [B][F][k] per-row top-k
+    float* tk_lp;
+    uint32_t* status;
+    int B, F, V, k, step, M;
+};
+struct RerankParams {
+    const int32_t* node_parent;
+    const int32_t* node_token;
+    const float* node_score;
+    int32_t* parents;                 // [B][N]
+    int32_t* tokens;
+    uint32_t* status;
+    int B, M, N;
+};
+cudaError_t launch_draft_step(const DraftParams& p, cudaStream_t s);
+cudaError_t launch_rerank(const RerankParams& p, cudaStream_t s);
 size_t attn_simt_smem_bytes(int dtype, int D, int R_block);
 
 }  // namespace treespec

@@ -1,0 +1,225 @@
+// Draft-tree construction: one beam-expansion step (tree_draft_step) and the final
+// rerank (tree_rerank).  Every scored candidate becomes a node; the k best of a step
+// form the next frontier; the rerank chooses among all nodes.
+//
+// Confidence of a draft path = product of its conditional probabilities ("EAGLE-2 &
+// Lookahead Decoding", section 4); in log space a node's score is its parent's score
+// plus its log-probability (float32).  Each step branches every frontier node into its
+// top-k tokens and keeps the k best candidates; the rerank keeps the root and the
+// N - 1 best nodes ("Speculative Decoding" (SGLang), EAGLE decoding: expansion with
+// speculative_eagle_topk per step, then rerank to speculative_num_draft_tokens).
+// Ties: lower token id within a row, lower candidate index (frontier f, rank r ->
+// f * k + r) across a step, lower node index in the rerank.
+#include <climits>
+
+#include "common.cuh"
+
+namespace treespec {
+
+namespace {
+
+constexpr int kTopkThreads = 256;
+
+// a ranks before b: larger value, or equal value and smaller index
+__device__ __forceinline__ bool before(float av, int at, float bv, int bt) {
+    return av > bv || (av == bv && at < bt);
+}
+
+// Top-k tokens of one frontier row.  Each warp keeps one sorted list spread over its
+// lanes (lane i holds rank i, i < k) and a copy of its k-th entry in every lane; the
+// lanes test their elements against that threshold with one ballot, and the rare
+// winners are inserted one at a time by shifting the list down a lane.  Then warp 0
+// ranks the warps' lists.  (With a private list per thread, some lane of a warp inserts
+// at almost every element and the warp runs the insertion nearly always.)
+template <bool VEC>
+__global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftParams p) {
+    constexpr int kWarps = kTopkThreads / 32;
+    __shared__ float sv[kWarps * kMaxTopk];
+    __shared__ int st[kWarps * kMaxTopk];
+    const int row = blockIdx.x;                           // b * F + f
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k = p.k;
+    const float* lp = p.logprobs + size_t(row) * p.V;
+    float wv = -INFINITY, tv = -INFINITY;                // this lane's list entry; the warp's k-th entry
+    int wt = INT_MAX, tt = INT_MAX;
+    auto consider = [&](float x, int t) {                 // called by all lanes together
+        unsigned m = __ballot_sync(0xffffffffu, before(x, t, tv, tt));
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const float nv = __shfl_sync(0xffffffffu, x, src);
+            const int nt = __shfl_sync(0xffffffffu, t, src);
+            if (!before(nv, nt, tv, tt)) continue;        // displaced by an earlier winner of this round
+            const float uv = __shfl_up_sync(0xffffffffu, wv, 1);
+            const int ut = __shfl_up_sync(0xffffffffu, wt, 1);
+            const bool from_above = lane > 0 && before(nv, nt, uv, ut);
+            const bool take_new = before(nv, nt, wv, wt);
+            if (lane < k) {
+                if (from_above) {
+                    wv = uv;
+                    wt = ut;
+                } else if (take_new) {
+                    wv = nv;
+                    wt = nt;
+                }
+            }
+            tv = __shfl_sync(0xffffffffu, wv, k - 1);
+            tt = __shfl_sync(0xffffffffu, wt, k - 1);
+        }
+    };
+    // four independent loads per lane in flight before they are consumed
+    constexpr int kU = 4;
+    if constexpr (VEC) {
+        for (int v0 = 0; v0 < p.V; v0 += kTopkThreads * 4 * kU) {
+            float4 x[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int v = v0 + (u * kTopkThreads + tid) * 4;
+                x[u] = v < p.V ? __ldg(reinterpret_cast<const float4*>(lp + v))
+                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int v = v0 + (u * kTopkThreads + tid) * 4;
+                const bool in = v < p.V;
+                consider(x[u].x, in ? v : INT_MAX);
+                consider(x[u].y, in ? v + 1 : INT_MAX);
+                consider(x[u].z, in ? v + 2 : INT_MAX);
+                consider(x[u].w, in ? v + 3 : INT_MAX);
+            }
+        }
+    } else {
+        for (int v0 = 0; v0 < p.V; v0 += kTopkThreads * kU) {
+            float x[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int v = v0 + u * kTopkThreads + tid;
+                x[u] = v < p.V ? __ldg(lp + v) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int v = v0 + u * kTopkThreads + tid;
+                consider(x[u], v < p.V ? v : INT_MAX);
+            }
+        }
+    }
+    if (lane < k) {
+        sv[warp * kMaxTopk + lane] = wv;
+        st[warp * kMaxTopk + lane] = wt;
+    }
+    __syncthreads();
+    if (warp == 0) {                                      // rank the kWarps * k entries
+        const int n = kWarps * k;
+        for (int c = lane; c < n; c += 32) {
+            const int ci = (c / k) * kMaxTopk + c % k;
+            int rank = 0;
+            for (int o = 0; o < n; ++o) {
+                const int oi = (o / k) * kMaxTopk + o % k;
+                rank += before(sv[oi], st[oi], sv[ci], st[ci]) ? 1 : 0;
+            }
+            if (rank < k) {
+                p.tk_tok[size_t(row) * k + rank] = st[ci];
+                p.tk_lp[size_t(row) * k + rank] = sv[ci];
+                if (st[ci] == INT_MAX) atomicOr(p.status, TREESPEC_STATUS_BAD_TOKEN);   // fewer than k usable values
+            }
+        }
+    }
+}
+
+// One warp per sequence: write the F * k candidates as nodes base + (f * k + r), and the
+// k best (ties: lower candidate index) as the next frontier, best first.
+__global__ void __launch_bounds__(32) draft_select_kernel(const DraftParams p) {
+    __shared__ float cs[kMaxFrontier * kMaxTopk];
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int k = p.k, F = p.F, nc = F * k;
+    int* par = p.node_parent + size_t(b) * p.M;
+    int* tok = p.node_token + size_t(b) * p.M;
+    float* sc = p.node_score + size_t(b) * p.M;
+    const int base = p.step == 0 ? 1 : 1 + k + (p.step - 1) * k * k;
+    for (int c = lane; c < nc; c += 32) {
+        const int f = c / k;
+        const int node = p.step == 0 ? 0 : p.frontier_in[size_t(b) * F + f];
+        const float parent_score = p.step == 0 ? 0.f : sc[node];
+        const float score = parent_score + p.tk_lp[(size_t(b) * F + f) * k + c % k];
+        cs[c] = score;
+        par[base + c] = node;
+        tok[base + c] = p.tk_tok[(size_t(b) * F + f) * k + c % k];
+        sc[base + c] = score;
+    }
+    __syncwarp();
+    for (int c = lane; c < nc; c += 32) {
+        int rank = 0;
+        for (int o = 0; o < nc; ++o) rank += before(cs[o], o, cs[c], c) ? 1 : 0;
+        if (rank < k) p.frontier_out[size_t(b) * k + rank] = base + c;
+    }
+    if (p.step == 0 && lane == 0) {
+        par[0] = -1;
+        tok[0] = -1;
+        sc[0] = 0.f;
+    }
+}
+
+// One CTA per sequence: keep the root and the N - 1 best nodes, numbered by original
+// index, parents remapped.
+__global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
+    __shared__ float s[kMaxDraftNodes];
+    __shared__ int par[kMaxDraftNodes];
+    __shared__ int kept[kMaxDraftNodes], newidx[kMaxDraftNodes];
+    const int b = blockIdx.x, tid = threadIdx.x, M = p.M, N = p.N;
+    for (int i = tid; i < M; i += blockDim.x) {
+        s[i] = p.node_score[size_t(b) * M + i];
+        int q = p.node_parent[size_t(b) * M + i];
+        if (i > 0 && (q < 0 || q >= i)) {                 // not a topologically ordered tree
+            atomicOr(p.status, TREESPEC_STATUS_BAD_PARENT);
+            q = 0;
+        }
+        par[i] = q;
+    }
+    __syncthreads();
+    for (int i = tid; i < M; i += blockDim.x) {
+        int rank = 0;
+        if (i > 0)
+            for (int j = 1; j < M; ++j) rank += before(s[j], j, s[i], i) ? 1 : 0;
+        kept[i] = i == 0 || rank < N - 1;
+    }
+    __syncthreads();
+    for (int i = tid; i < M; i += blockDim.x) {
+        int n = 0;
+        for (int j = 0; j < i; ++j) n += kept[j];
+        newidx[i] = n;                                    // root -> 0, kept nodes -> 1, 2, ...
+    }
+    __syncthreads();
+    for (int i = tid; i < M; i += blockDim.x) {
+        if (!kept[i]) continue;
+        const int ni = newidx[i];
+        int q = -1;
+        if (i > 0) {
+            q = par[i];
+            if (!kept[q]) {                               // parent dropped: only with positive log-probs
+                atomicOr(p.status, TREESPEC_STATUS_BAD_PARENT);
+                q = 0;
+            }
+            q = newidx[q];
+        }
+        p.parents[size_t(b) * N + ni] = q;
+        p.tokens[size_t(b) * N + ni] = p.node_token[size_t(b) * M + i];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_draft_step(const DraftParams& p, cudaStream_t s) {
+    const unsigned grid = unsigned(p.B) * unsigned(p.F);
+    if (p.V % 4 == 0) draft_topk_kernel<true><<<grid, kTopkThreads, 0, s>>>(p);
+    else draft_topk_kernel<false><<<grid, kTopkThreads, 0, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
+    draft_select_kernel<<<unsigned(p.B), 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rerank(const RerankParams& p, cudaStream_t s) {
+    rerank_kernel<<<unsigned(p.B), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace treespec

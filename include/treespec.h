@@ -259,6 +259,57 @@ int tree_kv_commit(void *k_pages, void *v_pages, const int32_t *page_table,
                    const treespec_attn_shape *shape,
                    void *workspace, size_t workspace_bytes, treespec_stream_t stream);
 
+/* ---------------------------------------------------------------- draft-tree build */
+
+/* Workspace bytes tree_draft_step / tree_rerank need (0 if the sizes are invalid). */
+size_t treespec_draft_workspace_bytes(int32_t batch, int32_t frontier, int32_t topk);
+
+/*
+ * tree_draft_step -- one expansion step of the draft tree ("EAGLE-2 & Lookahead
+ * Decoding", section 4: a path's confidence is the product of its conditional
+ * probabilities and only the most confident branches keep expanding; "Speculative
+ * Decoding" (SGLang), EAGLE decoding: speculative_eagle_topk children per expanded node
+ * and step, then a rerank over the candidates).
+ *
+ * Node arrays [B][max_nodes]: node 0 is the root (score 0).  Step s (0-based) expands a
+ * frontier of F nodes -- the root at step 0 (F = 1), else the frontier the previous step
+ * returned (F = topk) -- and every one of the F*topk candidates becomes a node:
+ * candidate c = f*topk + r (frontier row f, rank r) is node base + c, with base = 1 at
+ * step 0 and 1 + topk + (s-1)*topk*topk after that.
+ *   logprobs     [B][F][V] float32: the draft model's log-probabilities of the next token
+ *                after each frontier node, rows in frontier order (not NaN)
+ *   frontier_in  [B][F] int32: the previous step's frontier_out (unused at step 0)
+ *   frontier_out [B][topk] int32 out: the topk best candidates of this step, best first
+ * A frontier node's children are its topk tokens (ties: lower token id), scored parent
+ * score + log-probability in float32; ranking across the step breaks ties by the lower
+ * candidate index.  Step 0 also writes the root (parent -1, token -1, score 0).
+ * Limits: topk in 1..16, V >= topk, base + F*topk <= max_nodes <= 1024.  A row with
+ * fewer than topk non-NaN values sets TREESPEC_STATUS_BAD_TOKEN.
+ */
+int tree_draft_step(const float *logprobs, int32_t batch, int32_t frontier, int32_t vocab,
+                    int32_t topk, int32_t step, const int32_t *frontier_in,
+                    int32_t *node_parent, int32_t *node_token, float *node_score,
+                    int32_t max_nodes, int32_t *frontier_out,
+                    void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
+/*
+ * tree_rerank -- keep the draft tree's best num_nodes nodes (the SGLang page: after the
+ * expansion, reranking keeps the top speculative_num_draft_tokens nodes).
+ *
+ * From node arrays [B][max_nodes] (node 0 the root, every parent index smaller than its
+ * node's), keeps the root and the num_nodes - 1 non-root nodes with the highest score
+ * (ties: lower node index), numbered in increasing original index, and writes the tree
+ * tree_attn_verify and tree_accept take: tree_parents [B][num_nodes] (root -1) and
+ * draft_tokens [B][num_nodes].  A parent index that is not smaller than its node's, or
+ * a kept node whose parent was dropped (possible only with positive log-probabilities),
+ * is attached to the root and sets TREESPEC_STATUS_BAD_PARENT.
+ * Limits: 1 <= num_nodes <= min(64, max_nodes), max_nodes <= 1024.
+ */
+int tree_rerank(const int32_t *node_parent, const int32_t *node_token, const float *node_score,
+                int32_t batch, int32_t max_nodes, int32_t num_nodes,
+                int32_t *tree_parents, int32_t *draft_tokens,
+                void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
 /* ------------------------------------------------------------------------- helpers */
 
 /* Synchronise `stream` and copy the status word of a workspace used by the last call
