@@ -733,16 +733,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     __shared__ double redd[32], scan[NT / 32 + 1];
     __shared__ float redf[32];
     __shared__ int redi[32];
-    __shared__ int s_cur, s_len, s_action, s_child, s_found, s_cv0, s_chit;
+    __shared__ int s_cur, s_len, s_action, s_child, s_found;
     __shared__ float ch_lg[kMaxNodes], ch_q[kMaxNodes];     // target logit / draft prob of each child's token
-    __shared__ float cw[E];                                  // the crossing thread's bonus weights
-    __shared__ double s_cbase;
     __shared__ ClusterRed<CL> cred;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
     const int b = blockIdx.y, tid = threadIdx.x;
     const int N = p.N, V = p.V;
-    const int v0 = (rank * NT + tid) * E;                    // first token of this thread
+    const int lane = tid & 31, warp = tid >> 5;
+    // Token layout: warp w of CTA `rank` owns the contiguous range wbase .. wbase + 32 E,
+    // and element e of lane l is token wbase + (e / 4) * 128 + 4 l + e % 4: every
+    // warp-wide float4 load reads 512 contiguous bytes.
+    const int wbase = (rank * (NT / 32) + warp) * 32 * E;
+    auto tok_of = [&](int e) { return wbase + (e >> 2) * 128 + lane * 4 + (e & 3); };
     ClusterReducer<NT, CL> red{&cred, redd, redf, redi, 0};
 
     for (int c = tid; c < N; c += NT) {
@@ -760,8 +763,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     float r[E];
     // the draft row is read only where a child is rejected (and for the bonus draw), from
     // L1/L2, instead of being held in registers beside the target row
-    auto q_at = [&](const float* q, int e) -> float4 {
-        const int v = v0 + e;
+    auto q_at = [&](const float* q, int e) -> float4 {        // e a multiple of 4
+        const int v = tok_of(e);
         return v < V ? __ldg(reinterpret_cast<const float4*>(q + v)) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     const float* q_last = nullptr;                          // the draft row of the last visited node
@@ -773,9 +776,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         const float* lg = p.logits + row * V;
         const float* qr = STOCH ? p.probs + row * V : nullptr;
         q_last = qr;
-        if (STOCH && v0 < V) {                              // this thread's draft tokens, into L2 early
+        if (STOCH) {                                        // this warp's draft tokens, into L2 early
 #pragma unroll
-            for (int e = 0; e < E; e += 32) prefetch_line_l2(qr + v0 + e);
+            for (int m = 0; m < E / 32; ++m) {
+                const int v = wbase + (lane + 32 * m) * 32;    // one 128-byte line per lane
+                if (v < V) prefetch_line_l2(qr + v);
+            }
         }
         if (STOCH) {                                        // what the sibling tests below will need
             for (int c = tid; c < N; c += NT) {
@@ -789,7 +795,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         float piz = 0.f;                                    // a rescale of r still to apply (0: none)
 #pragma unroll
         for (int e = 0; e < E; e += 4) {
-            const int v = v0 + e;
+            const int v = tok_of(e);
             float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             if (v < V) x = __ldg(reinterpret_cast<const float4*>(lg + v));
             r[e] = x.x; r[e + 1] = x.y; r[e + 2] = x.z; r[e + 3] = x.w;
@@ -798,8 +804,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             float best = -INFINITY;
             int bi = 0x7fffffff;
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                if (r[e] > best) { best = r[e]; bi = v0 + e; }
+            for (int e = 0; e < E; ++e) {
+                const int v = tok_of(e);
+                if (v < V && (r[e] > best || (r[e] == best && v < bi))) { best = r[e]; bi = v; }
+            }
             amax = red.argmax(best, bi);
         } else {
             float m = -INFINITY;
@@ -919,7 +927,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             return make_float4(fmaxf(r[e] - q4.x, 0.f), fmaxf(r[e + 1] - q4.y, 0.f), fmaxf(r[e + 2] - q4.z, 0.f),
                                fmaxf(r[e + 3] - q4.w, 0.f));
         };
-        double total = 0.0, mine = 0.0;
+        double total = 0.0, wsum = 0.0;                      // wsum: this warp's weight
         for (int attempt = 0; attempt < 2; ++attempt) {
             float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -930,68 +938,64 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                 m4[2] += w4.z;
                 m4[3] += w4.w;
             }
-            mine = double((m4[0] + m4[1]) + (m4[2] + m4[3]));
-            total = red.sum(mine);
+            const double lane_sum = double((m4[0] + m4[1]) + (m4[2] + m4[3]));
+            wsum = __shfl_sync(0xffffffffu, warp_sum_d(lane_sum), 0);
+            total = red.sum(lane_sum);
             if (total > 0.0 || rej == 0 || unchanged) break;
             unchanged = true;                                // zero residual mass: keep r_{rej-1}
         }
-        double cta_total = 0.0;
-        const double pre_thread = block_exclusive_d<NT>(mine, scan);
-        // total of this CTA = last thread's exclusive prefix + its own share
-        if (tid == NT - 1) scan[NT / 32] = pre_thread + mine;
+        // each warp's interval of the cumulative weight, in token order: warps of this CTA,
+        // then the CTAs of the cluster
+        if (lane == 0) scan[warp] = wsum;
         __syncthreads();
-        cta_total = scan[NT / 32];
+        double pre_warp = 0.0, cta_total = 0.0;
+        for (int w2 = 0; w2 < NT / 32; ++w2) {
+            if (w2 < warp) pre_warp += scan[w2];
+            cta_total += scan[w2];
+        }
         double all = 0.0;
         const double pre_cta = red.exclusive(cta_total, &all);
-        const double thr = double(uni[0]) * total;
-        const double base = pre_cta + pre_thread;
+        const double thr = double(uni[0]) * all;
+        const double base = pre_cta + pre_warp;
         if (tid == 0 && rank == 0) s_found = 0;
-        if (tid == 0) s_chit = 0;
         cluster.sync();
-        if (base <= thr && thr < base + mine) {              // the crossing lies in this thread's tokens
+        if (base <= thr && thr < base + wsum) {              // warp-uniform: the crossing is in this warp
+            // walk the warp's 128-token chunks in order; in the chunk that crosses, a scan
+            // over the lanes' four tokens finds the lane, the lane finds the token
+            double run = base;
+            int v = -1, lnz = -1;
+            bool done = false;
 #pragma unroll
             for (int e = 0; e < E; e += 4) {
                 const float4 w4 = weight4(e);
-                cw[e] = w4.x;
-                cw[e + 1] = w4.y;
-                cw[e + 2] = w4.z;
-                cw[e + 3] = w4.w;
-            }
-            s_cbase = base;
-            s_cv0 = v0;
-            s_chit = 1;
-        }
-        __syncthreads();
-        if (s_chit && tid < 32) {
-            // warp 0 walks those tokens: lane l holds E/32 of them, in token order
-            constexpr int PL = E / 32;
-            double sl = 0.0;
-            int lnz = -1;
+                const float w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-            for (int u = 0; u < PL; ++u) {
-                const float w = cw[tid * PL + u];
-                sl += double(w);
-                if (w > 0.f) lnz = s_cv0 + tid * PL + u;
-            }
-            const double incl = warp_inclusive_scan_d(sl);
-            const unsigned pass = __ballot_sync(0xffffffffu, s_cbase + incl > thr);
-            int v = -1;
-            if (pass) {
-                const int L = __ffs(pass) - 1;
-                if (tid == L) {
-                    double run = s_cbase + (incl - sl);
+                for (int u = 0; u < 4; ++u)
+                    if (w[u] > 0.f) lnz = max(lnz, tok_of(e + u));
+                if (done) continue;
+                const double ls = ((double(w[0]) + double(w[1])) + double(w[2])) + double(w[3]);
+                const double incl = warp_inclusive_scan_d(ls);
+                const double ctot = __shfl_sync(0xffffffffu, incl, 31);
+                if (run + ctot > thr) {
+                    const unsigned pass = __ballot_sync(0xffffffffu, run + incl > thr);
+                    const int L = pass ? __ffs(pass) - 1 : 31;
+                    if (lane == L) {
+                        double rr = run + (incl - ls);
 #pragma unroll
-                    for (int u = 0; u < PL; ++u) {
-                        run += double(cw[tid * PL + u]);
-                        if (v < 0 && run > thr) v = s_cv0 + tid * PL + u;
+                        for (int u = 0; u < 4; ++u) {
+                            rr += double(w[u]);
+                            if (v < 0 && rr > thr) v = tok_of(e + u);
+                        }
                     }
+                    v = __shfl_sync(0xffffffffu, v, L);
+                    done = true;
                 }
-                v = __shfl_sync(0xffffffffu, v, L);
+                run += ctot;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lnz = max(lnz, __shfl_xor_sync(0xffffffffu, lnz, o));
-            if (tid == 0) {
-                p.bonus[b] = v >= 0 ? v : lnz;
+            if (lane == 0) {
+                p.bonus[b] = v >= 0 ? v : lnz;               // not found: rounding at a boundary
                 *cluster.map_shared_rank(&s_found, 0) = 1;
             }
         }
@@ -1004,10 +1008,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
 #pragma unroll
             for (int e = 0; e < E; e += 4) {
                 const float4 w4 = weight4(e);
-                if (w4.x > 0.f) last_nz = v0 + e;
-                if (w4.y > 0.f) last_nz = v0 + e + 1;
-                if (w4.z > 0.f) last_nz = v0 + e + 2;
-                if (w4.w > 0.f) last_nz = v0 + e + 3;
+                if (w4.x > 0.f) last_nz = max(last_nz, tok_of(e));
+                if (w4.y > 0.f) last_nz = max(last_nz, tok_of(e + 1));
+                if (w4.z > 0.f) last_nz = max(last_nz, tok_of(e + 2));
+                if (w4.w > 0.f) last_nz = max(last_nz, tok_of(e + 3));
             }
             const int ln = red.argmax(float(last_nz), last_nz);  // largest index with mass
             if (rank == 0 && tid == 0) p.bonus[b] = ln < 0 ? 0 : ln;
