@@ -236,12 +236,15 @@ def run_gpu(args):
     total_ms, value = job_throughput(world, K, t_start.elapsed_time(t_end), dev)
 
     # ---- end to end: per-step inputs from pinned host memory, results back to the host
+    # the target rows (and draft rows) stay in pinned host memory: the path-only accept walk
+    # reads the rows it visits in place over the CPU-GPU link; everything else is copied in
     host = dict(q=t(x.q, bf, pin=True), pt=t(x.page_table, pin=True), pl=t(x.prefix_lens, pin=True),
-                par=t(x.tree_parents, pin=True), lg=t(x.target_logits, pin=True), tok=t(x.draft_tokens, pin=True),
-                qp=None if w.greedy else t(x.draft_probs, pin=True), u=None if w.greedy else t(x.uniforms, pin=True))
+                par=t(x.tree_parents, pin=True), tok=t(x.draft_tokens, pin=True),
+                u=None if w.greedy else t(x.uniforms, pin=True))
+    rows_h = dict(lg=t(x.target_logits, pin=True), qp=None if w.greedy else t(x.draft_probs, pin=True))
     dst = dict(q=torch.empty_like(d["q"]), pt=torch.empty_like(d["pt"]), pl=torch.empty_like(d["pl"]),
-               par=torch.empty_like(d["par"]), lg=torch.empty_like(d["lg"]), tok=torch.empty_like(d["tok"]),
-               qp=None if w.greedy else torch.empty_like(d["qp"]), u=None if w.greedy else torch.empty_like(d["u"]))
+               par=torch.empty_like(d["par"]), tok=torch.empty_like(d["tok"]),
+               u=None if w.greedy else torch.empty_like(d["u"]), **rows_h)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     path_h = torch.empty(path.shape, dtype=path.dtype).pin_memory()
     alen_h = torch.empty(alen.shape, dtype=alen.dtype).pin_memory()
@@ -271,6 +274,9 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_total_ms, e2e_value = job_throughput(world, K2, e0.elapsed_time(e1), dev)
+    # host bytes the walk reads in place: at most the visited target rows and their draft rows
+    row_bytes = w.vocab * 4 * (1 if w.greedy else 2)
+    in_place = int((alen.to(torch.int64) + 1).sum().item()) * row_bytes
 
     # ---- KV commit of the accepted paths (not part of the step above): timed on the resident
     # pool with the accepted paths of the last step; it moves rows in place, so it runs last
@@ -371,6 +377,10 @@ def run_gpu(args):
         "mean_accept_len": round(float(lens.mean()), 3), "tokens_per_step": round(float(lens.mean()) + 1, 3),
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "h2d_read_in_place_bytes_per_step_max": in_place,
+                "note": "q, page table, lengths, parents, tokens, uniforms copied in from pinned host memory; "
+                        "target logits and draft probabilities stay pinned on the host and the accept walk "
+                        "reads the visited rows in place",
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "kv_commit": {"ms": round(commit_ms, 4), "bytes": commit_bytes,

@@ -109,6 +109,16 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     return s.cuda_stream
 
 
+def _need_rows(t: torch.Tensor, name: str, device) -> None:
+    """float32 rows on `device`, or in pinned host memory (read in place by the kernel)."""
+    if not ((t.is_cuda and t.device == device) or (t.device.type == "cpu" and t.is_pinned())):
+        raise ValueError(f"{name} must be on {device} or in pinned host memory")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be torch.float32, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device) -> None:
     if not t.is_cuda or t.device != device:
         raise ValueError(f"{name} must be on {device}")
@@ -206,14 +216,17 @@ def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms
                 workspace: Optional[torch.Tensor] = None, stream=None):
     """Accept walk; see include/treespec.h.  Returns (accept_path, accept_len, bonus_token).
 
-    mode: ACCEPT_AUTO, ACCEPT_ALL_ROWS or ACCEPT_PATH_ONLY (tree_accept_with_mode)."""
-    dev = target_logits.device
+    mode: ACCEPT_AUTO, ACCEPT_ALL_ROWS or ACCEPT_PATH_ONLY (tree_accept_with_mode).
+    target_logits and draft_probs may be device tensors or pinned host tensors: the
+    kernel reads host rows in place over the CPU-GPU link, and the path-only schedule
+    reads only the rows on each sequence's walk."""
+    dev = draft_tokens.device
     B, N, V = target_logits.shape
-    _need(target_logits, "target_logits", torch.float32, dev)
+    _need_rows(target_logits, "target_logits", dev)
     _need(draft_tokens, "draft_tokens", torch.int32, dev)
     _need(tree_parents, "tree_parents", torch.int32, dev)
     if temperature > 0:
-        _need(draft_probs, "draft_probs", torch.float32, dev)
+        _need_rows(draft_probs, "draft_probs", dev)
         _need(uniforms, "uniforms", torch.float32, dev)
     if accept_path is None:
         accept_path = torch.empty((B, N), dtype=torch.int32, device=dev)

@@ -203,6 +203,10 @@ size_t treespec_accept_workspace_bytes(int32_t batch, int32_t num_nodes, int32_t
  *   bonus_token   [B]       int32    out
  * Limits: N in 1..64, V in 1..2^30.  A draft token outside [0, V) is rejected and
  * flagged with TREESPEC_STATUS_BAD_TOKEN.
+ * target_logits and draft_probs may point to device memory or to host memory the device
+ * can address (pinned, e.g. from cudaHostAlloc): the kernels then read the rows in place
+ * over the CPU-GPU link, and the path-only schedule reads only the rows on each
+ * sequence's walk instead of all B*N of them.  The other arrays live on the device.
  */
 int tree_accept(const float *target_logits, const int32_t *draft_tokens,
                 const float *draft_probs, const int32_t *tree_parents,

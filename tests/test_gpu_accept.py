@@ -157,3 +157,20 @@ def test_monte_carlo_invariance_on_gpu(ts, cuda_device, mode):
         stat += float(((cnt - exp) ** 2 / exp).sum())
         dof += V - 1
     assert stats.chi2.sf(stat, dof) > 1e-3
+
+
+@pytest.mark.parametrize("name", ["c2_llama3_8b_bf16_greedy", "c3_llama2_7b_bf16_stoch@b2",
+                                  "c4_llama3_70b_bf16_t0.7@b2"])
+@pytest.mark.parametrize("mode", [1, 2])
+def test_rows_in_pinned_host_memory_match_device_rows(ts, cuda_device, name, mode):
+    x = gi.make_inputs(gen.get(name), with_attention=False)
+    d = accept_device_inputs(x, cuda_device)
+    want = ts.tree_accept(d["target_logits"], d["draft_tokens"], d["draft_probs"], d["tree_parents"],
+                          d["uniforms"], x.temperature, mode=mode)
+    host_lg = torch.from_numpy(np.ascontiguousarray(x.target_logits)).pin_memory()
+    host_q = None if x.draft_probs is None else torch.from_numpy(np.ascontiguousarray(x.draft_probs)).pin_memory()
+    got = ts.tree_accept(host_lg, d["draft_tokens"], host_q, d["tree_parents"], d["uniforms"], x.temperature,
+                         mode=mode)
+    torch.cuda.synchronize()
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
