@@ -242,37 +242,79 @@ def run_gpu(args):
                 par=t(x.tree_parents, pin=True), tok=t(x.draft_tokens, pin=True),
                 u=None if w.greedy else t(x.uniforms, pin=True))
     rows_h = dict(lg=t(x.target_logits, pin=True), qp=None if w.greedy else t(x.draft_probs, pin=True))
-    dst = dict(q=torch.empty_like(d["q"]), pt=torch.empty_like(d["pt"]), pl=torch.empty_like(d["pl"]),
-               par=torch.empty_like(d["par"]), tok=torch.empty_like(d["tok"]),
-               u=None if w.greedy else torch.empty_like(d["u"]), **rows_h)
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    path_h = torch.empty(path.shape, dtype=path.dtype).pin_memory()
-    alen_h = torch.empty(alen.shape, dtype=alen.dtype).pin_memory()
-    bonus_h = torch.empty(bonus.shape, dtype=bonus.dtype).pin_memory()
+    # two sets of device inputs and results: step s+1's inputs are copied in, and step s-1's
+    # results copied out, on a second stream while step s computes (every step's copies stay
+    # inside the timed region)
+    def dev_inputs():
+        return dict(q=torch.empty_like(d["q"]), pt=torch.empty_like(d["pt"]), pl=torch.empty_like(d["pl"]),
+                    par=torch.empty_like(d["par"]), tok=torch.empty_like(d["tok"]),
+                    u=None if w.greedy else torch.empty_like(d["u"]), **rows_h)
+
+    def dev_results():
+        return dict(out=torch.empty_like(out), path=torch.empty_like(path), alen=torch.empty_like(alen),
+                    bonus=torch.empty_like(bonus))
+
+    def host_results():
+        return {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in dev_results().items()}
+
+    dsts, outs, hres = [dev_inputs(), dev_inputs()], [dev_results(), dev_results()], [host_results(), host_results()]
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = sum(v.numel() * v.element_size() for v in (out_h, path_h, alen_h, bonus_h))
+    d2h = sum(v.numel() * v.element_size() for v in hres[0].values())
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+    for ev in computed + drained:
+        ev.record(stream)
 
-    def e2e_step():
-        for k, v in host.items():
-            if v is not None:
-                dst[k].copy_(v, non_blocking=True)
-        step(dst)
-        out_h.copy_(out, non_blocking=True)
-        path_h.copy_(path, non_blocking=True)
-        alen_h.copy_(alen, non_blocking=True)
-        bonus_h.copy_(bonus, non_blocking=True)
+    def copy_in(i):
+        copy_stream.wait_event(computed[i])                 # the last step on buffer i is done with it
+        with torch.cuda.stream(copy_stream):
+            for k, v in host.items():
+                if v is not None:
+                    dsts[i][k].copy_(v, non_blocking=True)
+        copied[i].record(copy_stream)
 
-    for _ in range(2):
-        e2e_step()
+    def compute(i):
+        stream.wait_event(copied[i])
+        stream.wait_event(drained[i])                        # its results buffer has been read out
+        inp, res = dsts[i], outs[i]
+        ts.tree_attn_verify(inp["q"], d["k"], d["v"], inp["pt"], inp["pl"], inp["par"], res["out"],
+                            kernel=args.attn_kernel, workspace=ws_a, stream=stream)
+        ts.tree_accept(inp["lg"], inp["tok"], inp["qp"], inp["par"], inp["u"], w.temperature,
+                       accept_path=res["path"], accept_len=res["alen"], bonus_token=res["bonus"],
+                       mode=args.accept_mode, workspace=ws_b, stream=stream)
+        computed[i].record(stream)
+
+    def copy_out(i):
+        copy_stream.wait_event(computed[i])
+        with torch.cuda.stream(copy_stream):
+            for k, v in outs[i].items():
+                hres[i][k].copy_(v, non_blocking=True)
+        drained[i].record(copy_stream)
+
+    def e2e_run(n):
+        copy_in(0)
+        for s_ in range(n):
+            i = s_ & 1
+            compute(i)
+            if s_ + 1 < n:
+                copy_in(i ^ 1)
+            copy_out(i)
+        stream.wait_event(drained[(n - 1) & 1])
+
+    e2e_run(2)
     torch.cuda.synchronize()
     K2 = max(3, min(K, 20))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K2):
-        e2e_step()
+    copy_stream.wait_event(e0)
+    e2e_run(K2)
     e1.record(stream)
     torch.cuda.synchronize()
+    path.copy_(outs[(K2 - 1) & 1]["path"])
+    alen.copy_(outs[(K2 - 1) & 1]["alen"])
     e2e_total_ms, e2e_value = job_throughput(world, K2, e0.elapsed_time(e1), dev)
     # host bytes the walk reads in place: at most the visited target rows and their draft rows
     row_bytes = w.vocab * 4 * (1 if w.greedy else 2)
@@ -378,9 +420,10 @@ def run_gpu(args):
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "h2d_read_in_place_bytes_per_step_max": in_place,
-                "note": "q, page table, lengths, parents, tokens, uniforms copied in from pinned host memory; "
-                        "target logits and draft probabilities stay pinned on the host and the accept walk "
-                        "reads the visited rows in place",
+                "note": "q, page table, lengths, parents, tokens, uniforms copied in from pinned host memory and "
+                        "attention output + accept results copied back, on a second stream overlapping the "
+                        "neighbouring steps' compute; target logits and draft probabilities stay pinned on "
+                        "the host and the accept walk reads the visited rows in place",
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "kv_commit": {"ms": round(commit_ms, 4), "bytes": commit_bytes,
