@@ -387,7 +387,7 @@ def run_gpu(args):
     attn_tflops = work["attn_flops"] / (t_attn * 1e-3) / 1e12
     t_hbm = work["attn_bytes"] / (hbm * 1e9)
     t_tc = work["attn_flops"] / (tf_sus * 1e12)
-    kernel_name = "attn_simt_kernel" if plan.kernel == 1 else "attn_tc_kernel"
+    kernel_name = {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_tc_pair_kernel"}[plan.kernel]
     traffic = recorded_traffic(w.name, kernel_name)
     if t_tc > t_hbm:
         roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": tf_sus, "unit": "TFLOP/s",

@@ -63,12 +63,13 @@ int check_attn_shape(const treespec_attn_shape* s) {
     if ((long long)s->max_pages_per_seq * s->page_size > (1ll << 30)) return TREESPEC_ERR_SHAPE;
     const long long R = (long long)s->num_nodes * (s->num_q_heads / s->num_kv_heads);
     if (R > 4096 || (long long)s->num_kv_heads * ((R + 63) / 64) > 65535) return TREESPEC_ERR_SHAPE;
-    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC) return TREESPEC_ERR_SHAPE;
+    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC_PAIR) return TREESPEC_ERR_SHAPE;
     if (s->num_splits < 0) return TREESPEC_ERR_SHAPE;
-    if (s->kernel == TREESPEC_KERNEL_TC) {
+    if (s->kernel == TREESPEC_KERNEL_TC || s->kernel == TREESPEC_KERNEL_TC_PAIR) {
         if (!attn_tc_supported(s->dtype, s->head_dim)) return TREESPEC_ERR_DTYPE;
         if ((long long)s->num_pool_pages * s->page_size >= (1ll << 31)) return TREESPEC_ERR_SHAPE;
     }
+    if (s->kernel == TREESPEC_KERNEL_TC_PAIR && ((R + 127) / 128) % 2 != 0) return TREESPEC_ERR_SHAPE;
     return TREESPEC_OK;
 }
 
@@ -80,8 +81,17 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
                        (long long)s.num_pool_pages * s.page_size < (1ll << 31);
     // Tensor cores for every bf16 / head_dim 128 shape: measured faster than the CUDA-core
     // kernel from 16 rows per kv head up (rows are padded to the 128-row MMA tile).
-    if (s.kernel == TREESPEC_KERNEL_TC || (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
-        p.kernel = TREESPEC_KERNEL_TC;
+    // The two-tile kernel only where it measured faster: its CTAs (one per pair of row
+    // blocks) fill the SMs in one wave while the one-tile kernel's would need two (32 x
+    // 8192 tokens, 64 q / 8 kv heads, 64 nodes: 0.129 ms against 0.134 at batch 8, 0.471
+    // against 0.441 at batch 32).
+    if (s.kernel == TREESPEC_KERNEL_TC || s.kernel == TREESPEC_KERNEL_TC_PAIR ||
+        (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
+        const long long blocks = (long long)s.batch * s.num_kv_heads * ((R + 127) / 128);
+        const bool paired = ((R + 127) / 128) % 2 == 0 && blocks / 2 <= sms && blocks > sms;
+        p.kernel = s.kernel == TREESPEC_KERNEL_TC ? TREESPEC_KERNEL_TC
+                   : (s.kernel == TREESPEC_KERNEL_TC_PAIR || paired) ? TREESPEC_KERNEL_TC_PAIR
+                                                                      : TREESPEC_KERNEL_TC;
         p.rows_per_block = 128;
     } else {
         p.kernel = TREESPEC_KERNEL_SIMT;
@@ -90,11 +100,13 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     p.row_blocks = (R + p.rows_per_block - 1) / p.rows_per_block;
     const long long max_tokens = (long long)s.max_pages_per_seq * s.page_size;
     const int tile = 128;                       // split sizes are multiples of every tile size
-    const long long units = (long long)s.batch * s.num_kv_heads * p.row_blocks;
+    const bool tc = p.kernel == TREESPEC_KERNEL_TC || p.kernel == TREESPEC_KERNEL_TC_PAIR;
+    const long long units = (long long)s.batch * s.num_kv_heads *
+                            (p.kernel == TREESPEC_KERNEL_TC_PAIR ? p.row_blocks / 2 : p.row_blocks);
     long long splits;
     if (s.num_splits > 0) {
         splits = s.num_splits;
-    } else if (p.kernel == TREESPEC_KERNEL_TC) {
+    } else if (tc) {
         // One CTA fits an SM.  Split a sequence only as far as filling the SMs once needs,
         // keep a CTA's run at most 66 tiles (a ragged batch's longest sequences split into
         // several CTAs; an 8256-token one stays whole), and no chunk below two tiles: each
@@ -114,7 +126,7 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     }
     long long chunk = (max_tokens + splits - 1) / splits;
     chunk = (chunk + tile - 1) / tile * tile;
-    if (s.num_splits == 0 && p.kernel != TREESPEC_KERNEL_TC && chunk > 16384) chunk = 16384;   // bounded CTA length
+    if (s.num_splits == 0 && !tc && chunk > 16384) chunk = 16384;   // bounded CTA length
     if (chunk < tile) chunk = tile;
     p.split_tokens = int(chunk);
     p.num_splits = int((max_tokens + chunk - 1) / chunk);
@@ -246,7 +258,9 @@ extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* 
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     if (launch_tree_prologue(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches++;
-    const cudaError_t e = plan.kernel == TREESPEC_KERNEL_TC ? launch_attn_tc(p, st) : launch_attn_simt(p, s.dtype, st);
+    const cudaError_t e = plan.kernel == TREESPEC_KERNEL_TC_PAIR ? launch_attn_tc_pair(p, st)
+                          : plan.kernel == TREESPEC_KERNEL_TC    ? launch_attn_tc(p, st)
+                                                                 : launch_attn_simt(p, s.dtype, st);
     if (e != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches++;
     if (plan.merge) {

@@ -4,23 +4,26 @@
 // computed with tcgen05:
 //   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
 //     are zero) x one split of the sequence's logical tokens, in 128-token tiles;
-//   * warp 0 streams the split's K pages (four-stage ring) and warp 10 its V pages
+//   * warp 0 streams the split's K pages (four-stage ring) and warp 6 its V pages
 //     (three stages) with TMA (one 16-token page x 64 head-dim columns per copy,
 //     128-byte swizzle; lanes 0-7 issue one page each); the partly filled last page
 //     of a sequence and pages past the split are written by the warp itself,
 //     zero-filled, so nothing outside the sequence reaches the MMA;
-//   * TMEM (512 columns, allocated by warp 1) holds two S buffers, Q and O; P_j is
-//     written over S_j.  Warp 1 issues S = Q K^T with Q read from TMEM, warp 11 issues
-//     O += P V with P read from TMEM, both as 128x128x16 tcgen05.mma instructions (two
-//     issuers, so that the barrier waits of one stream overlap the other's MMAs).  Only
-//     K and V pass through shared memory, whose bandwidth the MMAs and TMA share;
-//   * warps 2-9 (two per TMEM lane quarter, one query row per thread, each warp one
-//     half of the tile's columns) stage Q into TMEM, then per tile read S from TMEM,
+//   * TMEM (512 columns, allocated by warp 1) holds two S buffers, Q, one P buffer and
+//     O.  Warp 1 issues S = Q K^T with Q read from TMEM and O += P V with P read from
+//     TMEM, as 128x128x16 tcgen05.mma instructions, in the order S_0, S_1, P_0 V_0,
+//     S_2, P_1 V_1, S_3, ...: S_{j+2} reuses the buffer of S_j as soon as the softmax
+//     has read it, and the softmax of tile j+1 runs while the tensor pipe computes
+//     P_j V_j and S_{j+2}.  Only K and V pass through shared memory, whose bandwidth the
+//     MMAs and TMA share;
+//   * warps 2-5 (one per TMEM lane quarter, one query row per thread over all of the
+//     tile's columns, so a row's maximum needs no exchange between warps) stage Q into
+//     TMEM, then per tile read S from TMEM,
 //     apply the tree mask -- prefix tokens always, tree token S+j only when bit j of
 //     the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2 mask M
 //     and section 5 bitmask) -- run the online softmax in base 2, write P as packed
-//     bf16 back to TMEM, and rescale O in TMEM only when a row's running max grows by
-//     more than 2^8.
+//     bf16 into the P buffer once P_{j-1} V_{j-1} has read it, and rescale O in TMEM
+//     (after that MMA too) only when a row's running max grows by more than 2^8.
 // Every mbarrier wait is bounded; on expiry the CTA records TREESPEC_STATUS_TIMEOUT,
 // drains its own tensor-core work, frees TMEM and exits.
 #include <cuda.h>
@@ -42,13 +45,13 @@ constexpr int kNSK = 4;              // K ring stages
 constexpr int kNSV = 3;              // V ring stages
 constexpr int kPanel = 128 * 128;    // one [128 rows][64 bf16] swizzled panel, bytes
 constexpr int kTile = 2 * kPanel;    // [128][128] bf16
-constexpr int kThreads = 384;        // K producer, S issuer, 8 softmax warps, V producer, PV issuer
-constexpr int kWarpV = 10;           // the V producer warp
-constexpr int kWarpPV = 11;          // the P V issuer warp
+constexpr int kThreads = 224;        // K producer, MMA issuer, 4 softmax warps, V producer
+constexpr int kWarpV = 6;            // the V producer warp
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSB = 2;               // S buffers in TMEM: columns [0, 256); P_j overwrites S_j
+constexpr int kSB = 2;               // S buffers in TMEM: columns [0, 256)
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColQ = 256;      // Q (bf16 pairs): [256, 320)
+constexpr uint32_t kColP = 320;      // P (bf16 pairs): [320, 384)
 constexpr uint32_t kColO = 384;      // O: [384, 512)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -56,47 +59,15 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kNSK * kTile;
 constexpr int kOffBar = kOffV + kNSV * kTile;
-constexpr int kNumBars = 2 * kNSK + 2 * kNSV + 3 * kSB + 1 + 2 + 8;   // k/v full/empty, s_full, p_full, s_free, q_full, drain x2, xchg
+constexpr int kNumBars = 2 * kNSK + 2 * kNSV + 2 * kSB + 3;   // k/v full/empty, s_full, p_full, pv_done, q_full, drain
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffXch = kOffMisc + 16;                      // softmax half-row exchange, 2 x 2 x 128 floats
-constexpr int kOffAnc = kOffXch + 2 * 2 * 128 * 4;
-constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 232,200 bytes: within the 227 KB limit
+constexpr int kOffAnc = kOffMisc + 16;
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 230,072 bytes: within the 227 KB limit
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t k_full[kNSK], k_empty[kNSK], v_full[kNSV], v_empty[kNSV], s_full[kSB], p_full[kSB], s_free[kSB], q_full, drain[2], xchg[4][2];
+    uint64_t k_full[kNSK], k_empty[kNSK], v_full[kNSV], v_empty[kNSV], s_full[kSB], p_full[kSB], pv_done, q_full, drain;
 };
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// max of three floats in one instruction
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-// (d0, d1) = (a0 * b + c, a1 * b + c) as one packed f32x2 instruction
-__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b, float c) {
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b), "f"(c));
-}
-
-// (d0, d1) += (a0, a1) as one packed f32x2 instruction
-__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
-    asm("{\n\t.reg .b64 ra, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
-        "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1));
-}
 
 // CL > 1: the CL CTAs of a cluster hold consecutive row blocks of the same
 // (sequence, kv head, split); each issues the TMA copies of every CL-th page of a tile
@@ -154,14 +125,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kSB; ++s) {
             mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->p_full[s], 256);
-            mbar_init(&bars->s_free[s], 1);
+            mbar_init(&bars->p_full[s], kM);
         }
-        mbar_init(&bars->q_full, 256);
-        mbar_init(&bars->drain[0], 1);
-        mbar_init(&bars->drain[1], 1);
+        mbar_init(&bars->pv_done, 1);
+        mbar_init(&bars->q_full, kM);
+        mbar_init(&bars->drain, 1);
         *abort_flag = 0;
-        for (int f = 0; f < 8; ++f) mbar_init(&bars->xchg[f >> 1][f & 1], 2);
         fence_mbar_init();
     }
     for (int e = tid; e < p.N; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N + e];
@@ -180,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kWarpV) {
         // ------------------------------------------------------------ TMA producers
-        // warp 0 streams K (4 stages), warp 10 streams V (3 stages): a K stage is free again
+        // warp 0 streams K (4 stages), warp 6 streams V (3 stages): a K stage is free again
         // as soon as S of its tile has been computed, a V stage only after P V.
         const bool is_v = warp == kWarpV;
         const int nst = is_v ? kNSV : kNSK;                 // ring stages
@@ -274,103 +243,85 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1 || warp == kWarpPV) {
-        // ------------------------------------------------------------ MMA issuers
-        // Two independent streams into the CTA's tensor pipe: warp 1 issues S_j = Q K_j^T,
-        // warp 11 issues O += P_j V_j.  They share no TMEM columns and no ring, so the
-        // barrier waits of one overlap the other's MMAs instead of draining the pipe.
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop (all lanes wait, so control flow stays uniform) and
-        // one elected lane issues each group of MMAs with its commits.  Each scheduler also
-        // runs two busy softmax warps: issue code in a one-lane branch measured 108 cycles
-        // per 128x128x16 MMA beside them, the warp-uniform form 69 (64 alone).
-        {
-            const bool pv = warp == kWarpPV;
-            // both barriers of a step tested back to back, then waited (bounded) if needed;
-            // the verdict is made warp-uniform
-            auto ready2 = [&](uint64_t* x, uint32_t px, uint64_t* y, uint32_t py) -> bool {
-                const bool rx = mbar_try_wait(x, px);
-                const bool ry = mbar_try_wait(y, py);
-                bool r = rx && ry;
-                if (!__all_sync(0xffffffffu, r)) {
-                    r = !*abort_flag && (rx || mbar_wait_bounded(x, px, kWaitNs)) &&
-                        (ry || mbar_wait_bounded(y, py, kWaitNs));
-                }
-                return __all_sync(0xffffffffu, r);
-            };
-            bool ok = true;
-            if (!pv) {
-                constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
-                // Q is read from TMEM (written there by the softmax warps), K from the ring;
-                // a K-step or a stage moves only the start-address field of the K descriptor
-                // (address >> 4 in the low 14 bits, which no offset in the window overflows)
-                const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->q_full, 0, kWaitNs));
-                for (int j = 0; ok && j < ntiles; ++j) {
-                    const int stage = j % kNSK;
-                    // K_j has landed; S buffer j%2 is free once P_{j-2} V_{j-2} has read it
-                    const int sb = j % kSB;
-                    ok = j >= kSB ? ready2(&bars->k_full[stage], (j / kNSK) & 1, &bars->s_free[sb], ((j / kSB) - 1) & 1)
-                                  : __all_sync(0xffffffffu, mbar_wait_bounded(&bars->k_full[stage], (j / kNSK) & 1, kWaitNs));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t kb = dk + uint64_t((stage * kTile) >> 4);
-                    const uint32_t d = tbase + kColS + uint32_t(sb) * 128u;
-                    if (elect_one()) {
-#pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk) {   // 16 head dims = 8 packed columns of Q
-                            const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
-                            mma_bf16_ts(d, tbase + kColQ + kk * 8, kb + koff, kIdS, kk > 0);
-                        }
-                        if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
-                        else mma_commit_multicast(&bars->k_empty[stage], kMask);
-                        mma_commit(&bars->s_full[sb]);
-                    }
-                    __syncwarp();
-                }
-            } else {
-                constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
-                const uint64_t dv = smem_desc(sbase + kOffV, kPanel, 1024);
-                for (int j = 0; ok && j < ntiles; ++j) {
-                    const int stage = j % kNSV;
-                    // P_j is in TMEM; V_j has landed
-                    const int sb = j % kSB;
-                    ok = ready2(&bars->p_full[sb], (j / kSB) & 1, &bars->v_full[stage], (j / kNSV) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t vb = dv + uint64_t((stage * kTile) >> 4);
-                    // P_j sits in S_j's buffer: tokens 0-63 in columns [0, 32), tokens 64-127 in
-                    // [64, 96) (each softmax warp overwrites only its own half of S)
-                    const uint32_t pcol = tbase + kColS + uint32_t(sb) * 128u;
-                    if (elect_one()) {
-#pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk) {  // 16 tokens = 8 packed columns of P
-                            mma_bf16_ts(tbase + kColO, pcol + (kk >> 2) * 64 + (kk & 3) * 8,
-                                        vb + uint64_t((kk * 2048) >> 4), kIdO, (j > 0 || kk > 0));
-                        }
-                        if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
-                        else mma_commit_multicast(&bars->v_empty[stage], kMask);
-                        mma_commit(&bars->s_free[sb]);
-                    }
-                    __syncwarp();
-                }
+        // one elected lane issues each group of MMAs with its commits (issue code in a
+        // one-lane branch measured 108 cycles per 128x128x16 MMA beside busy softmax
+        // warps, the warp-uniform form 69; 64 alone).
+        auto ready2 = [&](uint64_t* x, uint32_t px, uint64_t* y, uint32_t py) -> bool {
+            const bool rx = mbar_try_wait(x, px);
+            const bool ry = mbar_try_wait(y, py);
+            bool r = rx && ry;
+            if (!__all_sync(0xffffffffu, r)) {
+                r = !*abort_flag && (rx || mbar_wait_bounded(x, px, kWaitNs)) &&
+                    (ry || mbar_wait_bounded(y, py, kWaitNs));
             }
-            if (!ok && lane == 0) {
-                *abort_flag = 1;
-                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+            return __all_sync(0xffffffffu, r);
+        };
+        constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
+        constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
+        // Q is read from TMEM (written there by the softmax warps), K and V from the rings;
+        // a K-step or a stage moves only the start-address field of a descriptor (address
+        // >> 4 in the low 14 bits, which no offset in the window overflows)
+        const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
+        const uint64_t dv = smem_desc(sbase + kOffV, kPanel, 1024);
+        // S_j into buffer j % 2 (the softmax has read S_{j-2} from it: p_full of tile j-2)
+        auto issue_s = [&](int j) -> bool {
+            const int stage = j % kNSK, sb = j % kSB;
+            const bool ok = j >= kSB ? ready2(&bars->k_full[stage], (j / kNSK) & 1, &bars->p_full[sb], ((j / kSB) - 1) & 1)
+                                     : ready2(&bars->k_full[stage], (j / kNSK) & 1, &bars->k_full[stage], (j / kNSK) & 1);
+            if (!ok) return false;
+            tc_fence_after();
+            const uint64_t kb = dk + uint64_t((stage * kTile) >> 4);
+            const uint32_t d = tbase + kColS + uint32_t(sb) * 128u;
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {   // 16 head dims = 8 packed columns of Q
+                    const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
+                    mma_bf16_ts(d, tbase + kColQ + kk * 8, kb + koff, kIdS, kk > 0);
+                }
+                if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
+                else mma_commit_multicast(&bars->k_empty[stage], kMask);
+                mma_commit(&bars->s_full[sb]);
             }
-            uint64_t* drain = &bars->drain[pv ? 1 : 0];
-            if (elect_one()) mma_commit(drain);             // the pipe completes MMAs in issue order
             __syncwarp();
-            mbar_wait_bounded(drain, 0, kWaitNs);
+            return true;
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->q_full, 0, kWaitNs));
+        for (int j = 0; ok && j < kSB && j < ntiles; ++j) ok = issue_s(j);
+        for (int j = 0; ok && j < ntiles; ++j) {
+            // O += P_j V_j once P_j is in TMEM and V_j has landed, then S_{j+2}
+            const int stage = j % kNSV;
+            ok = ready2(&bars->p_full[j % kSB], (j / kSB) & 1, &bars->v_full[stage], (j / kNSV) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t vb = dv + uint64_t((stage * kTile) >> 4);
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)     // 16 tokens = 8 packed columns of P
+                    mma_bf16_ts(tbase + kColO, tbase + kColP + kk * 8, vb + uint64_t((kk * 2048) >> 4), kIdO,
+                                (j > 0 || kk > 0));
+                if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
+                else mma_commit_multicast(&bars->v_empty[stage], kMask);
+                mma_commit(&bars->pv_done);
+            }
+            __syncwarp();
+            if (j + kSB < ntiles) ok = issue_s(j + kSB);
         }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+        }
+        if (elect_one()) mma_commit(&bars->drain);          // the pipe completes MMAs in issue order
+        __syncwarp();
+        mbar_wait_bounded(&bars->drain, 0, kWaitNs);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Eight warps: warp w owns TMEM lane quarter (w % 4) = 32 query rows, and one
-        // half of the tile's columns (warps 2-5: columns 0-63, warps 6-9: 64-127).  The
-        // two warps of a quarter swap their half-row maxima through shared memory.
+        // Four warps: warp w owns TMEM lane quarter (w % 4) = 32 query rows, one row per
+        // thread over all 128 columns of a tile.
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;                    // 0 or 1
         const int t = quarter * 32 + lane;                   // query row in the block = TMEM lane
         const int r = r0 + t;
         const bool row_ok = r < p.R;
@@ -379,54 +330,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t anc = row_ok ? anc_s[i] : 0ull;
         const bool warp_rows = __any_sync(0xffffffffu, row_ok);
         const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
-        float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2 slot][2 half][128 rows]
-        // Swap one float per row with the other half's warp of this quarter (both sit on
-        // the same scheduler): write the value, arrive on the quarter's barrier of slot
-        // seq&1 (two arrivals per phase); collect waits for that phase, sleeping in
-        // hardware, and reads the partner's value.  Slot seq&1 is rewritten at seq+2 only
-        // after the partner's arrival for seq+1, which follows its collect of seq.
-        auto publish = [&](float value, int seq) {
-            xch[((seq & 1) * 2 + half) * 128 + t] = value;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->xchg[quarter][seq & 1]);
-        };
-        auto collect = [&](int seq, bool* ok) -> float {
-            *ok = mbar_wait_bounded(&bars->xchg[quarter][seq & 1], ((seq - 1) >> 1) & 1, kWaitNs);
-            return xch[((seq & 1) * 2 + (half ^ 1)) * 128 + t];
-        };
         {
-            // this row's 64 head dims of Q into TMEM as 32 bf16 pairs (the A operand of S)
+            // this row of Q into TMEM as 64 bf16 pairs (the A operand of S)
             const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                               ((size_t(b) * p.N + i) * p.Hq + hq) * kD) + half * 8;
-            uint32_t qv[32];
+                                                               ((size_t(b) * p.N + i) * p.Hq + hq) * kD);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 w = row_ok ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
-                qv[4 * c] = w.x;
-                qv[4 * c + 1] = w.y;
-                qv[4 * c + 2] = w.z;
-                qv[4 * c + 3] = w.w;
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 w = row_ok ? __ldg(qsrc + hh * 8 + c) : make_uint4(0, 0, 0, 0);
+                    qv[4 * c] = w.x;
+                    qv[4 * c + 1] = w.y;
+                    qv[4 * c + 2] = w.z;
+                    qv[4 * c + 3] = w.w;
+                }
+                tmem_st32(tl + kColQ + hh * 32, qv);
+                tmem_wait_st();
             }
-            tmem_st32(tl + kColQ + half * 32, qv);
-            tmem_wait_st();
         }
         tc_fence_before();
         mbar_arrive(&bars->q_full);
 
         const float sc = p.scale_log2;
-        float m_used = -INFINITY, l = 0.f;                   // l: this warp's half of the row sum
+        float m_used = -INFINITY, l = 0.f;
         bool alive = true;
-        uint32_t v[kBN / 2];
-        for (int j = 0; j < ntiles && alive; ++j) {
+        uint32_t v[kBN];
+        for (int j = 0; j < ntiles; ++j) {
             const int base = t0 + j * kBN;
-            // which of this half's 64 columns the row may see, as two 32-bit words: prefix
+            // which of the tile's 128 columns the row may see, as four 32-bit words: prefix
             // columns below pref_end, tree columns [tree_lo, tree_hi) via the ancestor word
             const int pref_end = min(S, t1) - base;
             const int tree_lo = S - base, tree_hi = t1 - base;
-            uint32_t mw[2];
+            uint32_t mw[4];
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                const int lo = 64 * half + 32 * w;
+            for (int w = 0; w < 4; ++w) {
+                const int lo = 32 * w;
                 const int np = min(max(pref_end - lo, 0), 32);
                 uint32_t bits = np == 32 ? 0xffffffffu : ((1u << np) - 1u);
                 const int nh = min(max(tree_hi - lo, 0), 32);
@@ -438,119 +377,93 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bits |= tb & hi_mask;
                 mw[w] = row_ok ? bits : 0u;
             }
-            const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
+            const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu);
             const int sb = j % kSB;
-            const uint32_t scol = tl + kColS + uint32_t(sb) * 128u + half * 64;
-            // S of this half-row into v, masked columns set to -inf
-            auto load_s = [&]() {
-                if (warp_rows) {
-                    tmem_ld32(scol, v);
-                    tmem_ld32(scol + 32, v + 32);
-                    tmem_wait_ld();
-                }
-                constexpr uint32_t kNegInf = 0xff800000u;
-                if (!full) {
-#pragma unroll
-                    for (int c = 0; c < kBN / 2; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
-                }
-            };
-            // probabilities 2^(s*scale - msub), rounded to bf16 and packed in pairs in place
-            // (pair c overwrites v[c], whose value was read at pair c/2); returns their sum
-            auto exps = [&](float msub) -> float {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-                for (int c = 0; c < kBN / 4; ++c) {
-                    float x0, x1;
-                    fma_f32x2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), sc, -msub);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    v[c] = pack_bf16x2(p0, p1);
-                    if (c & 1) add_f32x2(a2, a3, p0, p1);
-                    else add_f32x2(a0, a1, p0, p1);
-                }
-                return (a0 + a1) + (a2 + a3);
-            };
+            const uint32_t scol = tl + kColS + uint32_t(sb) * 128u;
             if (!mbar_wait_bounded(&bars->s_full[sb], (j / kSB) & 1, kWaitNs)) { alive = false; break; }
             tc_fence_after();
-            load_s();
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(scol + c * 32, v + c * 32);
+                tmem_wait_ld();
+            }
+            if (!full) {
+                constexpr uint32_t kNegInf = 0xff800000u;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
+            }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kBN / 2; c += 8) {
+            for (int c = 0; c < kBN; c += 8) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     mx[e] = fmax3(mx[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
             }
-            const float mhalf = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
-            publish(mhalf, j + 1);
-            // Speculate that the running max stays: the exponentials taken now are final
-            // unless some row's max over both halves rises more than 8 above m_used.
-            const bool spec = __all_sync(0xffffffffu, mhalf * sc <= m_used + 8.f);
-            float lsum = 0.f;
-            if (spec) lsum = exps(m_used == -INFINITY ? 0.f : m_used);
-            // the row's max over both halves (identical in the two warps of the quarter)
-            bool xok = true;
-            const float mt = fmaxf(mhalf, collect(j + 1, &xok)) * sc;   // scale > 0 commutes with max
-            if (!xok) { alive = false; break; }
+            const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sc;   // scale > 0 commutes with max
             bool resc = false;
             float alpha = 1.f;
-            const bool grow = mt > m_used + 8.f;
-            if (grow) {
+            if (mt > m_used + 8.f) {
                 alpha = ex2(m_used - mt);
                 resc = m_used != -INFINITY;
                 l *= alpha;
                 m_used = mt;
             }
-            if (!spec || __any_sync(0xffffffffu, grow)) {
-                if (spec) load_s();                        // v holds P: S is still in TMEM
-                lsum = exps(m_used == -INFINITY ? 0.f : m_used);
-            }
-            l += lsum;
-            if (__any_sync(0xffffffffu, resc)) {
-                // O may only be rescaled once P_{j-1} V_{j-1} is in it (this warp's 64 columns)
-                if (!mbar_wait_bounded(&bars->s_free[(j - 1) % kSB], ((j - 1) / kSB) & 1, kWaitNs)) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after();
-                const float f = resc ? alpha : 1.f;
+            // probabilities 2^(s*scale - m_used), rounded to bf16 and packed in pairs in place
+            // (pair c overwrites v[c], whose value was read at pair c/2)
+            const float msub = m_used == -INFINITY ? 0.f : m_used;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kBN / 2; ++c) {
+                float x0, x1;
+                fma_f32x2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), sc, -msub);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                v[c] = pack_bf16x2(p0, p1);
+                if (c & 1) add_f32x2(a2, a3, p0, p1);
+                else add_f32x2(a0, a1, p0, p1);
+            }
+            l += (a0 + a1) + (a2 + a3);
+            // the P buffer and O are free once P_{j-1} V_{j-1} has completed
+            if (j > 0 && !mbar_wait_bounded(&bars->pv_done, (j - 1) & 1, kWaitNs)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            if (warp_rows) {
+                tmem_st32(tl + kColP, v);
+                tmem_st32(tl + kColP + 32, v + 32);
+            }
+            tmem_wait_st();
+            if (__any_sync(0xffffffffu, resc)) {
+                const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tl + kColO + half * 64 + c * 32, o);
+                    tmem_ld32(tl + kColO + c * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st32(tl + kColO + half * 64 + c * 32, o);
+                    tmem_st32(tl + kColO + c * 32, o);
+                    tmem_wait_st();
                 }
             }
-            tc_fence_after();
-            if (warp_rows) tmem_st32(scol, v);             // P over the first 32 columns of this half of S
-            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full[sb]);
         }
-        if (!alive) {
+        if (!alive || !mbar_wait_bounded(&bars->pv_done, (ntiles - 1) & 1, kWaitNs)) {
             *abort_flag = 1;
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-        } else if (mbar_wait_bounded(&bars->s_free[(ntiles - 1) % kSB], ((ntiles - 1) / kSB) & 1, kWaitNs)) {
+        } else {
             tc_fence_after();
-            // the row sum over both halves
-            bool xok = true;
-            publish(l, ntiles + 1);
-            const float lrow = l + collect(ntiles + 1, &xok);
-            if (!xok) {
-                *abort_flag = 1;
-                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-            }
-            const float inv = 1.f / lrow;
+            const float inv = 1.f / l;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
                 if (warp_rows) {
-                    tmem_ld32(tl + kColO + half * 64 + c * 32, o);
+                    tmem_ld32(tl + kColO + c * 32, o);
                     tmem_wait_ld();
                 }
                 if (!row_ok) continue;
-                const int col0 = half * 64 + c * 32;
+                const int col0 = c * 32;
                 if (!p.merge) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
                                                           ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);
@@ -571,15 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 8; ++e)
                         dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
                                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-                    if (c == 0 && half == 0) {
+                    if (c == 0) {
                         p.part_ml[pr * 2] = m_used;
-                        p.part_ml[pr * 2 + 1] = lrow;
+                        p.part_ml[pr * 2 + 1] = l;
                     }
                 }
             }
-        } else {
-            *abort_flag = 1;
-            atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
         }
     }
 
@@ -590,7 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (CL > 1) cluster_sync_all();      // no peer still writes into this CTA
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* ptr = nullptr;
@@ -618,8 +530,6 @@ bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_t
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool attn_tc_supported(int dtype, int D) { return dtype == TREESPEC_DTYPE_BF16 && D == kD; }
 

@@ -1,0 +1,539 @@
+// Split-KV paged tree attention on the 5th-generation tensor cores, two query tiles
+// per CTA (bf16, head_dim 128, an even number of 128-row blocks per kv head).
+//
+// Same partial state as the other kernels (m, l, acc per query row of one split).  One
+// CTA holds 256 query rows of one kv head as two 128-row query tiles (row r = node i * G
+// + g) and one split of the sequence's logical tokens, in 64-token KV tiles:
+//   * shared memory: Q of both query tiles (written once by the softmax warps, 128-byte
+//     swizzle), a five-stage K ring (warp 8) and a five-stage V ring (warp 9) filled by
+//     TMA one 16-token page x 64 head dims per copy; the partly filled last page of a
+//     sequence and pages past the split are written by the producer warp itself,
+//     zero-filled;
+//   * TMEM (all 512 columns): for each query tile t two 64-column S buffers and O_t;
+//     P_t(j) is written over the first 32 columns of S buffer j % 2 as packed bf16;
+//   * warp 10 issues the MMAs of query tile 0 and warp 11 those of tile 1, in the order
+//     S_t(0), S_t(1), P_t(0) V(0), S_t(2), P_t(1) V(1), ...: S of the next KV tile is
+//     computed while the softmax works on the current one, and S_t(j) reuses buffer
+//     j % 2 only after P_t(j-2) V(j-2) has completed;
+//   * warps 0-3 run the softmax of query tile 0 and warps 4-7 that of tile 1, one query
+//     row per thread over all columns of a KV tile (the row maximum needs no exchange
+//     between warps).  Per KV tile: read S from TMEM, apply the tree mask -- prefix
+//     tokens always, tree token S+j only when bit j of the node's ancestor word is set
+//     ("Tech Radar: SGLang EAGLE-2", section 2 mask M and section 5 bitmask) -- take the
+//     online softmax in base 2, rescale O in TMEM only when a row's running max grows by
+//     more than 2^8 (after P_t(j-1) V(j-1) has completed), and write P back to TMEM.
+// Every mbarrier wait is bounded; on expiry the CTA records TREESPEC_STATUS_TIMEOUT,
+// drains its own tensor-core work, frees TMEM and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace treespec {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kM = 128;              // query rows per tile = TMEM lanes
+constexpr int kNQ = 2;               // query tiles per CTA
+constexpr int kD = 128;              // head dim
+constexpr int kBN = 64;              // tokens per KV tile
+constexpr int kPages = kBN / 16;     // 16-token pages per KV tile
+constexpr int kNSK = 5;              // K ring stages
+constexpr int kNSV = 5;              // V ring stages
+constexpr int kQPanel = kM * 128;    // one [128 rows][64 bf16] swizzled panel of Q, bytes
+constexpr int kQTile = 2 * kQPanel;  // [128][128] bf16
+constexpr int kPanel = kBN * 128;    // one [64 tokens][64 bf16] swizzled panel of K or V
+constexpr int kTile = 2 * kPanel;    // [64][128] bf16
+constexpr int kThreads = 384;        // 8 softmax warps, K producer, V producer, 2 MMA issuers
+constexpr int kWarpK = 8;
+constexpr int kWarpV = 9;
+constexpr int kWarpMma = 10;         // warps 10 and 11 issue the MMAs of tiles 0 and 1
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;        // S buffer b of tile t: [128 t + 64 b, 128 t + 64 b + 64)
+constexpr uint32_t kColO = 256;      // O_t: [256 + 128 t, 256 + 128 t + 128)
+constexpr uint64_t kWaitNs = 2000000000ull;
+// registers per thread: 168 at launch (384 threads); then the producer / issuer
+// warpgroup (warps 8-11) drops to 56 and the two softmax warpgroups rise to 200:
+// 128 x (200 + 200 + 56) = 58,368 <= 384 x 168 = 64,512
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 56;
+static_assert(128 * (2 * kRegsSoftmax + kRegsOther) <= kThreads * 168, "register split exceeds the launch allocation");
+
+// shared-memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kNQ * kQTile;
+constexpr int kOffV = kOffK + kNSK * kTile;
+constexpr int kOffBar = kOffV + kNSV * kTile;
+
+struct Bars {
+    uint64_t k_full[kNSK], k_empty[kNSK], v_full[kNSV], v_empty[kNSV];
+    uint64_t q_full[kNQ], s_full[kNQ][2], p_full[kNQ][2], pv_done[kNQ][2], o_full[kNQ], drain[kNQ];
+};
+constexpr int kOffMisc = kOffBar + int(sizeof(Bars));
+constexpr int kOffAnc = kOffMisc + 16;
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;         // 230,208 bytes
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// CL > 1: the CL CTAs of a cluster hold consecutive row-block pairs of the same
+// (sequence, kv head, split); each issues the TMA copies of every CL-th page of a tile
+// multicast to all of them, and a stage is refilled only after both tiles of all CL
+// CTAs released it.
+template <int CL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_pair_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+    volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
+    uint64_t* anc_s = reinterpret_cast<uint64_t*>(sm + kOffAnc);
+
+    const int pairs = p.row_blocks / kNQ;
+    const int split = blockIdx.x;
+    const int h = blockIdx.y / pairs, pr = blockIdx.y % pairs;
+    const int b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = pr * kNQ * kM;
+    const int S = p.lens[b];
+
+    if (S < 0) {                                   // invalid sequence: zeros (or the merge writes them)
+        if (!p.merge && split == 0) {
+            for (int e = tid; e < kNQ * kM * (kD / 8); e += kThreads) {
+                const int row = r0 + e / (kD / 8), c = e % (kD / 8);
+                if (row >= p.R) continue;
+                const int i = row / p.G, hq = h * p.G + row % p.G;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                      ((size_t(b) * p.N + i) * p.Hq + hq) * kD) + c;
+                *dst = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+    const int L = S + p.N;
+    const int t0 = split * p.split_tokens;
+    const int t1 = min(L, t0 + p.split_tokens);
+    if (t0 >= t1) return;
+    const int ntiles = (t1 - t0 + kBN - 1) / kBN;
+    if (smem_u32(sm) & 1023u) {                    // never expected; refuse rather than misread tiles
+        if (tid == 0) atomicOr(p.status, TREESPEC_STATUS_INTERNAL);
+        return;
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < kNSK; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], kNQ * CL);
+        }
+        for (int s = 0; s < kNSV; ++s) {
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], kNQ * CL);
+        }
+        for (int t = 0; t < kNQ; ++t) {
+            mbar_init(&bars->q_full[t], kM);
+            for (int bf = 0; bf < 2; ++bf) {
+                mbar_init(&bars->s_full[t][bf], 1);
+                mbar_init(&bars->p_full[t][bf], kM);
+                mbar_init(&bars->pv_done[t][bf], 1);
+            }
+            mbar_init(&bars->o_full[t], 1);
+            mbar_init(&bars->drain[t], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int e = tid; e < p.N; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N + e];
+    if (warp == kWarpMma) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if constexpr (CL > 1) cluster_sync_all();      // peers' barriers exist before any multicast
+    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+    constexpr uint16_t kMask = uint16_t((1u << CL) - 1u);
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+    if (warp >= kWarpK) {
+      // one setmaxnreg for the whole warpgroup, then its producer or issuer role
+      regs_lower<kRegsOther>();
+      if (warp == kWarpK || warp == kWarpV) {
+        // ------------------------------------------------------------ TMA producers
+        const bool is_v = warp == kWarpV;
+        const int nst = is_v ? kNSV : kNSK;
+        uint64_t* full = is_v ? bars->v_full : bars->k_full;
+        uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
+        const uint16_t* src = static_cast<const uint16_t*>(is_v ? p.v : p.k);
+        const CUtensorMap* map = is_v ? &tmv : &tmk;
+        unsigned char* ring = sm + (is_v ? kOffV : kOffK);
+        const int* ptab = p.page_table + size_t(b) * p.max_pages;
+        if (lane == 0) tma_prefetch_desc(map);
+        // page ids in batches of eight tiles (lane l: page l & 3 of tile 8 * batch + (l >> 2)),
+        // fetched a batch ahead
+        auto fetch_batch = [&](int bi) -> int {
+            const int jt = 8 * bi + (lane >> 2);
+            const int pos0 = t0 + jt * kBN + (lane & 3) * 16;
+            return (jt < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
+        };
+        int batch_cur = fetch_batch(0), batch_next = fetch_batch(1);
+        for (int j = 0; j < ntiles; ++j) {
+            const int stage = j % nst;
+            if (j > 0 && (j & 7) == 0) {
+                batch_cur = batch_next;
+                batch_next = fetch_batch((j >> 3) + 1);
+            }
+            int page = __shfl_sync(0xffffffffu, batch_cur, ((j & 7) << 2) | (lane & 3));
+            const int base = t0 + j * kBN;
+            // lanes 0..3 own page `lane` of the tile: 1 = full page by TMA, 2 = written here
+            const int pos0 = base + lane * 16;
+            int kind = 0;
+            if (lane < kPages) {
+                kind = 2;
+                if (pos0 < t1) {
+                    const bool ok = page >= 0 && page < p.num_pool_pages;
+                    if (!ok) atomicOr(p.status, TREESPEC_STATUS_BAD_PAGE);
+                    if (ok && pos0 + 16 <= L) kind = 1;
+                    if (!ok) page = -1;
+                } else {
+                    page = -1;
+                }
+            }
+            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+            }
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            unsigned char* dst = ring + stage * kTile;
+            const unsigned manual = __ballot_sync(0xffffffffu, kind == 2);
+            if (manual) {
+                for (int pg = 0; pg < kPages; ++pg) {
+                    if (!((manual >> pg) & 1u)) continue;
+                    const int pgid = __shfl_sync(0xffffffffu, page, pg);
+                    const int q0 = base + pg * 16;
+                    for (int c = lane; c < 16 * 16; c += 32) {      // 16 token rows x 16 chunks of 16 bytes
+                        const int rr = c >> 4, ch = c & 15;
+                        const int pos = q0 + rr;
+                        uint4 val = make_uint4(0, 0, 0, 0);
+                        if (pgid >= 0 && pos < t1) {
+                            const size_t off = ((size_t(pgid) * p.ps + (pos & 15)) * p.Hkv + h) * kD + ch * 8;
+                            val = __ldg(reinterpret_cast<const uint4*>(src + off));
+                        }
+                        *reinterpret_cast<uint4*>(dst + (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7)) = val;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
+            if (lane == 0) mbar_arrive_expect_tx(&full[stage], uint32_t(__popc(viatma)) * 2u * 2048u);
+            __syncwarp();
+            if (kind == 1 && (CL == 1 || (lane % CL) == int(rank))) {   // each page's two copies
+                const int z = page * 16;
+                if constexpr (CL == 1) {
+                    tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
+                    tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
+                } else {
+                    tma_load_3d_multicast(dst + lane * 2048, map, 0, h, z, &full[stage], kMask);
+                    tma_load_3d_multicast(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage], kMask);
+                }
+            }
+            __syncwarp();
+        }
+        if constexpr (CL > 1) {
+            // every peer's release of every stage has landed here before this CTA may exit
+            for (int s2 = 0; s2 < nst && s2 < ntiles; ++s2) {
+                const int uses = (ntiles - s2 + nst - 1) / nst;
+                if (!mbar_wait_bounded(&empty[s2], (uses - 1) & 1, kWaitNs)) {
+                    *abort_flag = 1;
+                    atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+                }
+            }
+        }
+      } else {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 10 + t issues every MMA of tile t.  The whole warp runs the loop (all lanes
+        // wait, so control flow stays uniform); one elected lane issues each group and its
+        // commits.
+        const int t = warp - kWarpMma;
+        auto ready = [&](uint64_t* x, uint32_t px) -> bool {
+            bool r = mbar_try_wait(x, px);
+            if (!__all_sync(0xffffffffu, r)) r = !*abort_flag && (r || mbar_wait_bounded(x, px, kWaitNs));
+            return __all_sync(0xffffffffu, r);
+        };
+        constexpr uint32_t kIdS = idesc_bf16_f32(128, kBN, false);
+        constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
+        const uint32_t dS = tbase + kColS + uint32_t(t) * 128u;
+        const uint32_t dO = tbase + kColO + uint32_t(t) * 128u;
+        // a K-step or a stage moves only the start-address field of a descriptor
+        // (address >> 4 in the low 14 bits, which no offset in the window overflows)
+        const uint64_t dq = smem_desc(sbase + kOffQ + t * kQTile, 16, 1024);
+        const uint64_t dk = smem_desc(sbase + kOffK, 16, 1024);
+        const uint64_t dv = smem_desc(sbase + kOffV, kPanel, 1024);
+        bool ok = ready(&bars->q_full[t], 0);
+        for (int j = 0; ok && j <= ntiles; ++j) {
+            if (j < ntiles) {
+                // S_t(j) = Q_t K(j)^T into buffer j % 2, once K(j) has landed and P_t(j-2) V(j-2)
+                // has read that buffer
+                const int ks = j % kNSK, bf = j & 1;
+                ok = ready(&bars->k_full[ks], (j / kNSK) & 1) &&
+                     (j < 2 || ready(&bars->pv_done[t][bf], ((j >> 1) - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t kb = dk + uint64_t((ks * kTile) >> 4);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t qoff = uint64_t(((kk >> 2) * kQPanel + (kk & 3) * 32) >> 4);
+                        const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
+                        mma_bf16_ss(dS + bf * 64u, dq + qoff, kb + koff, kIdS, kk > 0);
+                    }
+                    if constexpr (CL == 1) mma_commit(&bars->k_empty[ks]);
+                    else mma_commit_multicast(&bars->k_empty[ks], kMask);
+                    mma_commit(&bars->s_full[t][bf]);
+                }
+                __syncwarp();
+            }
+            if (j > 0) {
+                // O_t += P_t(j-1) V(j-1): P in the first 32 columns of buffer (j-1) % 2
+                const int jp = j - 1, vs = jp % kNSV, bf = jp & 1;
+                ok = ready(&bars->p_full[t][bf], (jp >> 1) & 1) && ready(&bars->v_full[vs], (jp / kNSV) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t vb = dv + uint64_t((vs * kTile) >> 4);
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)     // 16 tokens = 8 packed columns of P
+                        mma_bf16_ts(dO, dS + bf * 64u + kk * 8, vb + uint64_t((kk * 2048) >> 4), kIdO,
+                                    (jp > 0 || kk > 0));
+                    if constexpr (CL == 1) mma_commit(&bars->v_empty[vs]);
+                    else mma_commit_multicast(&bars->v_empty[vs], kMask);
+                    mma_commit(&bars->pv_done[t][bf]);
+                    if (jp == ntiles - 1) mma_commit(&bars->o_full[t]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+        }
+        if (elect_one()) mma_commit(&bars->drain[t]);      // the pipe completes MMAs in issue order
+        __syncwarp();
+        mbar_wait_bounded(&bars->drain[t], 0, kWaitNs);
+        __syncwarp();
+      }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        regs_raise<kRegsSoftmax>();
+        const int t = warp >> 2;                             // query tile
+        const int quarter = warp & 3;                        // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;                 // row in the tile = TMEM lane
+        const int r = r0 + t * kM + row;
+        const bool row_ok = r < p.R;
+        const int i = row_ok ? r / p.G : 0;
+        const int hq = h * p.G + (row_ok ? r % p.G : 0);
+        const uint64_t anc = row_ok ? anc_s[i] : 0ull;
+        const bool warp_rows = __any_sync(0xffffffffu, row_ok);
+        const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
+        const uint32_t scol0 = tl + kColS + uint32_t(t) * 128u;
+        const uint32_t ocol = tl + kColO + uint32_t(t) * 128u;
+        {
+            // this row of Q into the tile's swizzled shared-memory image (the A operand of S)
+            const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                               ((size_t(b) * p.N + i) * p.Hq + hq) * kD);
+            unsigned char* qt = sm + kOffQ + t * kQTile;
+#pragma unroll
+            for (int ch = 0; ch < kD / 8; ++ch) {
+                const uint4 w = row_ok ? __ldg(qsrc + ch) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(qt + (ch >> 3) * kQPanel + sw128_offset(row, ch & 7)) = w;
+            }
+            fence_proxy_async_smem();
+        }
+        mbar_arrive(&bars->q_full[t]);
+
+        const float sc = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool alive = true;
+        uint32_t v[kBN];
+        for (int j = 0; j < ntiles; ++j) {
+            const int base = t0 + j * kBN;
+            const int bf = j & 1;
+            const uint32_t scol = scol0 + bf * 64u;
+            // which of the tile's columns the row may see, as 32-bit words: prefix columns
+            // below pref_end, tree columns [tree_lo, tree_hi) via the ancestor word
+            const int pref_end = min(S, t1) - base;
+            const int tree_lo = S - base, tree_hi = t1 - base;
+            uint32_t mw[kBN / 32];
+#pragma unroll
+            for (int w = 0; w < kBN / 32; ++w) {
+                const int lo = 32 * w;
+                const int np = min(max(pref_end - lo, 0), 32);
+                uint32_t bits = np == 32 ? 0xffffffffu : ((1u << np) - 1u);
+                const int nh = min(max(tree_hi - lo, 0), 32);
+                const uint32_t hi_mask = nh == 32 ? 0xffffffffu : ((1u << nh) - 1u);
+                uint32_t tb = 0;
+                const int sh = lo - tree_lo;               // anc bit index of column lo
+                if (sh >= 0) tb = sh < 64 ? uint32_t(anc >> sh) : 0u;
+                else tb = -sh < 32 ? uint32_t(anc << (-sh)) : 0u;
+                bits |= tb & hi_mask;
+                mw[w] = row_ok ? bits : 0u;
+            }
+            const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
+            if (!mbar_wait_bounded(&bars->s_full[t][bf], (j >> 1) & 1, kWaitNs)) { alive = false; break; }
+            tc_fence_after();
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) tmem_ld32(scol + c * 32, v + c * 32);
+                tmem_wait_ld();
+            }
+            if (!full) {
+                constexpr uint32_t kNegInf = 0xff800000u;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < kBN; c += 8) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    mx[e] = fmax3(mx[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
+            }
+            const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sc;   // scale > 0 commutes with max
+            bool resc = false;
+            float alpha = 1.f;
+            if (mt > m_used + 8.f) {
+                alpha = ex2(m_used - mt);
+                resc = m_used != -INFINITY;
+                l *= alpha;
+                m_used = mt;
+            }
+            // probabilities 2^(s*scale - m_used), rounded to bf16 and packed in pairs in place
+            // (pair c overwrites v[c], whose value was read at pair c/2)
+            const float msub = m_used == -INFINITY ? 0.f : m_used;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN / 2; ++c) {
+                float x0, x1;
+                fma_f32x2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), sc, -msub);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                v[c] = pack_bf16x2(p0, p1);
+                if (c & 1) add_f32x2(a2, a3, p0, p1);
+                else add_f32x2(a0, a1, p0, p1);
+            }
+            l += (a0 + a1) + (a2 + a3);
+            if (warp_rows) tmem_st32(scol, v);             // P over the first 32 columns of the buffer
+            tmem_wait_st();
+            if (__any_sync(0xffffffffu, resc)) {
+                // O_t may be rescaled once P_t(j-1) V(j-1) is in it (P_t(j) V(j) waits for p_full)
+                if (!mbar_wait_bounded(&bars->pv_done[t][bf ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                const float f = resc ? alpha : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(ocol + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tmem_st32(ocol + c * 32, o);
+                    tmem_wait_st();                        // frees o[] before the next chunk
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[t][bf]);
+        }
+        if (!alive || !mbar_wait_bounded(&bars->o_full[t], 0, kWaitNs)) {
+            *abort_flag = 1;
+            atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
+        } else {
+            tc_fence_after();
+            const float inv = 1.f / l;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                if (warp_rows) {
+                    tmem_ld32(ocol + c * 32, o);
+                    tmem_wait_ld();
+                }
+                if (!row_ok) continue;
+                const int col0 = c * 32;
+                if (!p.merge) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                          ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k2 = 0; k2 < 4; ++k2) {
+                            const int idx = e * 8 + k2 * 2;
+                            w4[k2] = pack_bf16x2(__uint_as_float(o[idx]) * inv, __uint_as_float(o[idx + 1]) * inv);
+                        }
+                        dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                } else {
+                    const size_t prow = (size_t(b * p.Hkv + h) * p.num_splits + split) * p.R + r;
+                    float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * kD + col0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                             __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    if (c == 0) {
+                        p.part_ml[prow * 2] = m_used;
+                        p.part_ml[prow * 2 + 1] = l;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) tmem_dealloc(tbase, kTmemCols);
+    if constexpr (CL > 1) cluster_sync_all();      // no peer still writes into this CTA
+}
+
+template <int CL>
+cudaError_t launch_pair_cluster(const AttnParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s) {
+    auto kern = attn_tc_pair_kernel<CL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_splits, p.Hkv * (p.row_blocks / kNQ), p.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = CL;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Pairs of CTAs of one kv head (four row blocks) share each K/V copy when the head has
+// an even number of row-block pairs.
+int attn_tc_pair_cluster_size(int row_blocks) { return (row_blocks / kNQ) % 2 == 0 ? 2 : 1; }
+
+cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s) {
+    if (p.row_blocks % kNQ != 0 || p.rows_per_block != kM) return cudaErrorInvalidValue;
+    CUtensorMap mk, mv;
+    const long long pool_tokens = (long long)p.num_pool_pages * p.ps;
+    if (!make_pool_map(&mk, p.k, p.Hkv, pool_tokens) || !make_pool_map(&mv, p.v, p.Hkv, pool_tokens))
+        return cudaErrorInvalidValue;
+    if (attn_tc_pair_cluster_size(p.row_blocks) == 2) return launch_pair_cluster<2>(p, mk, mv, s);
+    return launch_pair_cluster<1>(p, mk, mv, s);
+}
+
+}  // namespace treespec

@@ -1,6 +1,7 @@
 // Shared device helpers and launch parameter blocks of libtreespec.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,7 +49,7 @@ struct AttnLayout {
 };
 
 struct AttnPlan {
-    int kernel;          // TREESPEC_KERNEL_SIMT / _TC
+    int kernel;          // TREESPEC_KERNEL_SIMT / _TC / _TC_PAIR
     int num_splits;
     int split_tokens;
     int rows_per_block;
@@ -102,8 +103,12 @@ struct AcceptParams {
 cudaError_t launch_tree_prologue(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s);
 bool attn_tc_supported(int dtype, int D);
 int attn_tc_cluster_size(int row_blocks);
+int attn_tc_pair_cluster_size(int row_blocks);
+// TMA map of a K or V page pool [P][16][Hkv][128] bf16, one page x 64 head dims per box
+bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_tokens);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptParams& p, int mode, cudaStream_t s, int* kernels);
 

@@ -245,6 +245,54 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ------------------------------------------------------------------ register split
+
+// Per-warpgroup register limits: every warp of a warpgroup executes the same one.  An
+// increase takes registers the CTA's other warpgroups gave back, out of the CTA's
+// launch allocation (threads x registers per thread at launch); the caller keeps the
+// sum of all limits within it.
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------------------ softmax arithmetic
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (d0, d1) = (a0 * b + c, a1 * b + c) as one packed f32x2 instruction
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (d0, d1) += (a0, a1) as one packed f32x2 instruction
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled panel
 // whose rows are 128 bytes (the layout TMA SWIZZLE_128B writes and UMMA SW128 reads).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {

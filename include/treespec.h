@@ -52,7 +52,10 @@ enum treespec_dtype {
 enum treespec_kernel {
     TREESPEC_KERNEL_AUTO = 0,  /* tensor-core kernel for bf16 with head_dim 128, else CUDA cores */
     TREESPEC_KERNEL_SIMT = 1,  /* CUDA-core split-KV kernel (any dtype) */
-    TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128) */
+    TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128), one 128-row query tile per CTA */
+    TREESPEC_KERNEL_TC_PAIR = 3,  /* the same with two 128-row query tiles per CTA (bf16, head_dim 128, an even
+                                     number of 128-row blocks ceil(N*G / 128)); the automatic choice when its CTAs
+                                     fit the SMs in one wave and the one-tile kernel's do not */
 };
 
 enum treespec_accept_mode {
@@ -100,8 +103,8 @@ typedef struct {
 } treespec_attn_shape;
 
 typedef struct {
-    int32_t kernel;             /* the kernel the call will run (SIMT or TC) */
-    int32_t num_splits;         /* KV splits per (sequence, kv head, row block) */
+    int32_t kernel;             /* the kernel the call will run (SIMT, TC or TC_PAIR) */
+    int32_t num_splits;         /* KV splits per (sequence, kv head, row block or pair of them) */
     int32_t split_tokens;       /* logical tokens per split (a multiple of the tile) */
     int32_t rows_per_block;     /* query rows (node x group) one CTA holds */
     int32_t row_blocks;         /* ceil(N*G / rows_per_block) */

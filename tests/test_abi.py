@@ -46,6 +46,7 @@ def shape(**kw):
     dict(num_nodes=65), dict(num_nodes=0), dict(num_q_heads=30), dict(head_dim=96),
     dict(page_size=32), dict(batch=0), dict(dtype=7), dict(max_pages_per_seq=0),
     dict(num_splits=-1), dict(kernel=9),
+    dict(kernel=3),                       # two-tile kernel: 8 nodes x 4 query heads is one 128-row block
 ])
 def test_attention_rejects_bad_shapes(kw):
     prob = shape(**kw)
@@ -75,6 +76,20 @@ def test_plan_and_workspace_query():
     assert ts.attn_workspace_bytes(prob) > 0
     single = ts.attn_plan(shape(num_splits=1))
     assert single.num_splits == 1 and single.merge == 0
+
+
+def test_plan_pairs_query_tiles_for_one_wave():
+    """Without a device the planner assumes 152 SMs."""
+    wide = dict(num_nodes=64, num_q_heads=64, num_kv_heads=8)      # 512 rows: four 128-row blocks
+    b8 = ts.attn_plan(shape(batch=8, **wide))                      # 128 pair CTAs fit, 256 one-tile CTAs do not
+    assert b8.kernel == ts.KERNEL_TC_PAIR and b8.rows_per_block == 128 and b8.row_blocks == 4
+    assert ts.attn_plan(shape(batch=32, **wide)).kernel == ts.KERNEL_TC          # 512 pair CTAs: several waves
+    assert ts.attn_plan(shape(batch=1, **wide)).kernel == ts.KERNEL_TC           # splits fill the SMs anyway
+    assert ts.attn_plan(shape(batch=8, kernel=ts.KERNEL_TC, **wide)).kernel == ts.KERNEL_TC
+    assert ts.attn_plan(shape(batch=32, kernel=ts.KERNEL_TC_PAIR, **wide)).kernel == ts.KERNEL_TC_PAIR
+    assert ts.attn_plan(shape(batch=8, num_nodes=40, num_q_heads=64, num_kv_heads=8)).kernel == ts.KERNEL_TC
+    assert ts.attn_plan(shape()).kernel == ts.KERNEL_TC                                             # 32 rows
+    assert ts.attn_plan(shape(batch=8, dtype=ts.DTYPE_F32, **wide)).kernel == ts.KERNEL_SIMT
 
 
 def test_accept_rejects_bad_arguments():

@@ -37,14 +37,20 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2])
+def row_blocks(w):
+    return -(-w.num_nodes * w.group // 128)
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3])
 @pytest.mark.parametrize("name,batch", SMALL)
 def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
     w = gen.get(name)
     if batch is not None:
         w = w.with_batch(batch)
-    if kernel == 2 and w.dtype != "bf16":
-        pytest.skip("the tensor-core kernel takes bf16")
+    if kernel >= 2 and w.dtype != "bf16":
+        pytest.skip("the tensor-core kernels take bf16")
+    if kernel == 3 and row_blocks(w) % 2:
+        pytest.skip("the two-tile kernel needs an even number of 128-row blocks")
     x = gi.make_inputs(w, with_accept=False)
     out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
@@ -60,10 +66,10 @@ def test_auto_plan_picks_tensor_cores_for_bf16_head128(ts, cuda_device):
         assert ts.attn_plan(prob).kernel == want, name
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 @pytest.mark.parametrize("splits", [1, 3, 40])
 def test_split_counts(ts, cuda_device, kernel, splits):
-    w = gen.get("c2_llama3_8b_bf16_greedy")
+    w = gen.get("c2_llama3_8b_bf16_greedy") if kernel < 3 else gen.get("c4_llama3_70b_bf16_greedy").with_batch(1)
     x = gi.make_inputs(w, with_accept=False)
     out = run(ts, x, cuda_device, kernel=kernel, num_splits=splits)
     assert_attention_close(out, oracle_attention(x), w.dtype)
@@ -80,7 +86,8 @@ def _custom(name, parents, prefix, batch=None):
 
 
 @pytest.mark.parametrize("dtype_cfg,kernel", [("c1_tiny_f32_greedy", 1), ("c2_llama3_8b_bf16_greedy", 1),
-                                              ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2)])
+                                              ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2),
+                                              ("c4_llama3_70b_bf16_greedy", 3)])
 @pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
                                   "random64", "random32"])
 def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
@@ -100,6 +107,8 @@ def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
     else:
         parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
     w, x = _custom(dtype_cfg, parents, prefix)
+    if kernel == 3 and row_blocks(w) % 2:
+        pytest.skip("the two-tile kernel needs an even number of 128-row blocks")
     out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
 
@@ -161,6 +170,26 @@ def test_full_size_ragged_sampled(ts, cuda_device):
     out = run(ts, x, cuda_device)
     order = np.argsort(x.prefix_lens)
     pairs = [(int(order[0]), 0), (int(order[-1]), 7), (int(order[len(order) // 2]), 3)]
+    ref = oracle_attention(x, pairs)
+    mask = ~np.isnan(ref)
+    assert_attention_close(out, ref, w.dtype, mask=mask)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_two_tile_kernel_refuses_an_odd_number_of_row_blocks(ts, cuda_device):
+    w = gen.get("c2_llama3_8b_bf16_greedy")           # 8 nodes x 4 query heads: one 128-row block
+    x = gi.make_inputs(w, with_accept=False)
+    with pytest.raises((ValueError, ts.TreespecError)):
+        run(ts, x, cuda_device, kernel=ts.KERNEL_TC_PAIR)
+
+
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_full_size_tensor_core_kernels_agree(ts, cuda_device, kernel):
+    """Both tensor-core kernels on the full bench workload, checked on sampled pairs."""
+    w = gen.get("c4_llama3_70b_bf16_greedy")
+    x = gi.make_inputs(w, with_accept=False)
+    out = run(ts, x, cuda_device, kernel=kernel)
+    pairs = [(0, 0), (w.batch - 1, w.num_kv_heads - 1), (w.batch // 2, 3)]
     ref = oracle_attention(x, pairs)
     mask = ~np.isnan(ref)
     assert_attention_close(out, ref, w.dtype, mask=mask)
