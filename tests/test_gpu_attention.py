@@ -194,3 +194,33 @@ def test_full_size_tensor_core_kernels_agree(ts, cuda_device, kernel):
     mask = ~np.isnan(ref)
     assert_attention_close(out, ref, w.dtype, mask=mask)
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("kernel", [2, 3])
+@pytest.mark.parametrize("splits", [1, 0])
+def test_tensor_core_kernels_flag_bad_lengths_and_pages(ts, cuda_device, kernel, splits):
+    """An invalid sequence gets zero rows (written by the kernel itself with one split, by
+    the merge otherwise) and the other sequences stay exact; a bad page id is flagged."""
+    w = gen.get("c4_llama3_70b_bf16_greedy").with_batch(2)
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    prob = ts.attn_problem(d["q"], d["k_pages"], d["page_table"], kernel=kernel, num_splits=splits)
+    assert ts.attn_plan(prob).kernel == kernel
+    ws = torch.empty(ts.attn_workspace_bytes(prob), dtype=torch.uint8, device=cuda_device)
+    bad_len = d["prefix_lens"].clone()
+    bad_len[1] = 10 ** 6
+    out = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], bad_len, d["tree_parents"],
+                              kernel=kernel, num_splits=splits, workspace=ws)
+    torch.cuda.synchronize()
+    assert ts.read_status(ws) & 4
+    assert torch.all(out[1] == 0)
+    ref = oracle_attention(x, [(0, 0), (0, 5)])
+    mask = ~np.isnan(ref)
+    mask[1] = False
+    assert_attention_close(out, ref, w.dtype, mask=mask)
+    bad_pages = d["page_table"].clone()
+    bad_pages[0, 3] = 1 << 30
+    ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], bad_pages, d["prefix_lens"], d["tree_parents"],
+                        kernel=kernel, num_splits=splits, workspace=ws)
+    torch.cuda.synchronize()
+    assert ts.read_status(ws) & 2
