@@ -101,3 +101,16 @@ def random_root_path(parents: np.ndarray, rng: np.random.Generator, stop_prob: f
         cur = int(rng.choice(kids[cur]))
         path.append(cur)
     return path
+
+
+PAD = -2    # parent entry of a padding slot past the end of a smaller tree
+
+
+def padded(parent_rows, num_nodes: int) -> np.ndarray:
+    """Stack trees of different sizes into one [B][num_nodes] parent array, each row
+    padded with PAD after its own nodes."""
+    out = np.full((len(parent_rows), num_nodes), PAD, dtype=np.int32)
+    for b, row in enumerate(parent_rows):
+        row = np.asarray(row, dtype=np.int32)
+        out[b, : len(row)] = row
+    return out

@@ -36,7 +36,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .tree_mask import children, validate_parents
+from .tree_mask import children, tree_size, validate_parents
 
 
 @dataclass
@@ -124,7 +124,8 @@ def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms
     """Batch form of the walk.
 
     Returns (accept_path [B][N] int32, -1 padded; accept_len [B]; bonus_token [B];
-    list of WalkResult).
+    list of WalkResult).  A parent row padded with ABSENT is walked as its first
+    tree_size entries; the padding slots' rows are not read.
     """
     B, N = np.asarray(draft_tokens).shape
     path = np.full((B, N), -1, dtype=np.int32)
@@ -132,11 +133,12 @@ def tree_accept(target_logits, draft_tokens, draft_probs, tree_parents, uniforms
     bonus = np.zeros(B, dtype=np.int32)
     results = []
     for b in range(B):
+        nb = tree_size(tree_parents[b])
         if temperature == 0:
-            w = greedy_walk(target_logits[b], draft_tokens[b], tree_parents[b])
+            w = greedy_walk(target_logits[b][:nb], draft_tokens[b][:nb], tree_parents[b][:nb])
         else:
-            w = stochastic_walk(target_logits[b], draft_tokens[b], draft_probs[b],
-                                tree_parents[b], uniforms[b], temperature)
+            w = stochastic_walk(target_logits[b][:nb], draft_tokens[b][:nb], draft_probs[b][:nb],
+                                tree_parents[b][:nb], uniforms[b][:nb], temperature)
         path[b, : w.length] = w.path
         length[b] = w.length
         bonus[b] = w.bonus

@@ -10,7 +10,9 @@ Trees").  The query of node i, head hq, attends to
     T_i = {0 .. S-1}  U  {S + j : j in Ancestors(i) U {i}}
 
 where S is the sequence's prefix length and the N tree tokens occupy logical
-positions S .. S+N-1 in node order.  With h = hq // (Hq/Hkv) its kv head,
+positions S .. S+N-1 in node order.  A tree padded to the batch's node count
+(tree_mask.ABSENT entries) has N_b = tree_size nodes: its sequence is S + N_b
+tokens long and the rows of the padding slots are zero.  With h = hq // (Hq/Hkv) its kv head,
 
     s_t = q . K[t, h] / sqrt(D),   w = softmax(s over T_i),   out = sum_t w_t V[t, h].
 
@@ -25,7 +27,7 @@ from typing import Iterable, Optional
 
 import numpy as np
 
-from .tree_mask import mask_matrix
+from .tree_mask import mask_matrix, tree_size
 
 
 def gather_kv(pages, page_table_row, length: int, page_size: int, h: int) -> np.ndarray:
@@ -66,7 +68,8 @@ def tree_attention(q, k_pages, v_pages, page_table, prefix_lens, tree_parents,
 
     q [B][N][Hq][D], k_pages/v_pages [P][ps][Hkv][D] (float values of any
     precision, widened exactly to float64), page_table [B][max_pages],
-    prefix_lens [B], tree_parents [B][N].  Returns float64 [B][N][Hq][D].
+    prefix_lens [B], tree_parents [B][N] (rows may be padded with ABSENT).
+    Returns float64 [B][N][Hq][D].
     `pairs` restricts the work to the listed (b, kv head) pairs; other entries
     of the result are NaN.
     """
@@ -78,8 +81,10 @@ def tree_attention(q, k_pages, v_pages, page_table, prefix_lens, tree_parents,
         pairs = [(b, h) for b in range(B) for h in range(Hkv)]
     for b, h in pairs:
         S = int(prefix_lens[b])
-        K = gather_kv(k_pages, page_table[b], S + N, page_size, h)
-        V = gather_kv(v_pages, page_table[b], S + N, page_size, h)
-        q_bh = np.asarray(q[b, :, h * G:(h + 1) * G, :], dtype=np.float64)
-        out[b, :, h * G:(h + 1) * G, :] = tree_attention_head(q_bh, K, V, S, tree_parents[b])
+        nb = tree_size(tree_parents[b])
+        K = gather_kv(k_pages, page_table[b], S + nb, page_size, h)
+        V = gather_kv(v_pages, page_table[b], S + nb, page_size, h)
+        q_bh = np.asarray(q[b, :nb, h * G:(h + 1) * G, :], dtype=np.float64)
+        out[b, :nb, h * G:(h + 1) * G, :] = tree_attention_head(q_bh, K, V, S, tree_parents[b][:nb])
+        out[b, nb:, h * G:(h + 1) * G, :] = 0.0
     return out

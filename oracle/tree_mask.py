@@ -8,10 +8,32 @@ word with (1 << j).
 
 The tree arrives as a parent array in topological order: parents[0] = -1
 (the root, i.e. the last verified token) and 0 <= parents[i] < i.
+
+A batch may hold trees of different sizes ("EAGLE-2 & Lookahead Decoding",
+section 6, "Batched Dynamic Tree Slicing": the tree is cut to fewer tokens under
+load).  Reading: each row of the batch's parent array is padded to the batch's
+node count with ABSENT; a tree is the entries before its first ABSENT.
 """
 from __future__ import annotations
 
 import numpy as np
+
+
+ABSENT = -2     # parent entry of a padding slot past the end of a smaller tree
+
+
+def tree_size(parents) -> int:
+    """Number of nodes of a padded parent row: the entries before the first ABSENT.
+
+    The root must be present, and no present entry may follow an ABSENT one.
+    """
+    p = [int(x) for x in parents]
+    n = next((i for i, x in enumerate(p) if x == ABSENT), len(p))
+    if n == 0:
+        raise ValueError("the root (node 0) must be present")
+    if any(x != ABSENT for x in p[n:]):
+        raise ValueError("a present node follows an absent one")
+    return n
 
 
 def validate_parents(parents) -> None:

@@ -8,6 +8,7 @@ import torch
 from gen import inputs as gi
 from oracle import accept as oacc
 from oracle import attention as oatt
+from oracle.tree_mask import tree_size
 
 # Attention tolerances: float32 |err| <= 1e-4; bfloat16 |err| <= 1e-2 + 1e-2 |ref|.
 F32_ATOL = 1e-4
@@ -102,8 +103,10 @@ def compare_accept(gpu, logits, tokens, probs, parents, uniforms, temperature):
             continue
         assert results[b].min_margin < TIE_MARGIN, f"sequence {b}: gpu {got} != oracle {want}"
         ties += 1
-        alts = tie_alternatives(logits[b], tokens[b], None if probs is None else probs[b], parents[b],
-                                None if uniforms is None else uniforms[b], temperature, results[b])
+        nb = tree_size(parents[b])
+        alts = tie_alternatives(logits[b][:nb], tokens[b][:nb], None if probs is None else probs[b][:nb],
+                                parents[b][:nb], None if uniforms is None else uniforms[b][:nb], temperature,
+                                results[b])
         assert got in alts, f"sequence {b}: gpu {got} is not the oracle's {want} nor a tie neighbour"
         flipped += 1
     return len(olen), ties, flipped
