@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 DTYPE_F32, DTYPE_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC_PAIR = 0, 1, 2, 3
 ACCEPT_AUTO, ACCEPT_ALL_ROWS, ACCEPT_PATH_ONLY = 0, 1, 2
+ABSENT = -2                     # parent entry of a padding slot after a smaller tree
 STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT", 32: "INTERNAL",
                64: "BAD_PATH"}
 

@@ -381,10 +381,18 @@ __device__ int bonus_scan(BonusTerm term, int V, float u0) {
     return v < 0 ? 0 : v;
 }
 
+// Topological parent array, possibly padded with kAbsent after the tree's own nodes (a
+// batch may hold trees of different sizes); a padding slot is never anyone's child.
 __device__ __forceinline__ uint32_t check_parents(const int* par, int N) {
     uint32_t st = (par[0] != -1) ? TREESPEC_STATUS_BAD_PARENT : 0u;
-    for (int c = 1; c < N; ++c)
-        if (par[c] < 0 || par[c] >= c) st |= TREESPEC_STATUS_BAD_PARENT;
+    bool pad = false;
+    for (int c = 1; c < N; ++c) {
+        if (par[c] == kAbsent) {
+            pad = true;
+            continue;
+        }
+        if (pad || par[c] < 0 || par[c] >= c) st |= TREESPEC_STATUS_BAD_PARENT;
+    }
     return st;
 }
 
@@ -398,6 +406,7 @@ __global__ void __launch_bounds__(NT) accept_rows_kernel(AcceptParams p) {
     __shared__ float izs[kMaxNodes];
     const int row = blockIdx.x;                 // b * N + i
     const int b = row / p.N, i = row % p.N;
+    if (i > 0 && p.parents[row] == kAbsent) return;   // a padding slot's row is never visited
     const float* lg = p.logits + size_t(row) * p.V;
     if constexpr (!STOCH) {
         const int a = row_argmax<NT, VEC>(lg, p.V, redf, redi);

@@ -149,6 +149,8 @@ AttnLayout attn_layout(const treespec_attn_shape& s, const AttnPlan& p) {
     off = align_up(off + size_t(s.batch) * s.num_nodes * 8, kWsAlign);
     L.lens = off;
     off = align_up(off + size_t(s.batch) * 4, kWsAlign);
+    L.nn = off;
+    off = align_up(off + size_t(s.batch) * 4, kWsAlign);
     const size_t parts = p.merge ? size_t(s.batch) * s.num_kv_heads * p.num_splits * R : 0;
     L.ml = off;
     off = align_up(off + parts * 2 * 4, kWsAlign);
@@ -235,6 +237,7 @@ extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* 
     p.status = reinterpret_cast<uint32_t*>(ws + lay.status);
     p.anc = reinterpret_cast<uint64_t*>(ws + lay.anc);
     p.lens = reinterpret_cast<int32_t*>(ws + lay.lens);
+    p.nn = reinterpret_cast<int32_t*>(ws + lay.nn);
     p.part_ml = reinterpret_cast<float*>(ws + lay.ml);
     p.part_acc = reinterpret_cast<float*>(ws + lay.acc);
     p.B = s.batch;

@@ -28,8 +28,9 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(AttnParams p) {
     float acc[DS];
 #pragma unroll
     for (int e = 0; e < DS; ++e) acc[e] = 0.f;
-    if (S >= 0) {
-        const int L = S + p.N;
+    const int nb = p.nn[b];
+    if (S >= 0 && i < nb) {                // padding rows (nodes nb..) are zero
+        const int L = S + nb;
         const int nvalid = min(p.num_splits, (L + p.split_tokens - 1) / p.split_tokens);
         const size_t base = size_t(bh) * p.num_splits * p.R + row;   // + s * R
         float mm = -INFINITY;

@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnParams p) {
         }
         return;
     }
-    const int L = S + p.N;
+    const int nb = p.nn[b];               // rows of nodes nb.. are padding: zero output
+    const int L = S + nb;
     const int t0 = split * p.split_tokens;
     const int t1 = min(L, t0 + p.split_tokens);
     if (t0 >= t1) return;
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnParams p) {
         if (lr < rows) {
             int row = r0 + lr;
             int i = row / p.G, hq = h * p.G + row % p.G;
-            v = load_q<T>(p.q, ((size_t(b) * p.N + i) * p.Hq + hq) * D + d) * p.scale_log2;
+            if (i < nb) v = load_q<T>(p.q, ((size_t(b) * p.N + i) * p.Hq + hq) * D + d) * p.scale_log2;
         }
         Qs[e] = v;
     }
@@ -310,7 +311,8 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnParams p) {
         const int row = r0 + lr;
         if (!p.merge) {
             const int i = row / p.G, hq = h * p.G + row % p.G;
-            store_out<T>(p.out, ((size_t(b) * p.N + i) * p.Hq + hq) * D + d, a / lsum);
+            const bool present = i < *static_cast<volatile const int32_t*>(p.nn + b);   // re-read: not kept live
+            store_out<T>(p.out, ((size_t(b) * p.N + i) * p.Hq + hq) * D + d, present ? a / lsum : 0.f);
         } else {
             const size_t pr = (size_t(b * p.Hkv + h) * p.num_splits + split) * p.R + row;
             p.part_acc[pr * D + d] = a;

@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return;
     }
-    const int L = S + p.N;
+    const int nb = p.nn[b];                        // rows of nodes nb.. are padding: zero output
+    const int L = S + nb;
     const int t0 = split * p.split_tokens;
     const int t1 = min(L, t0 + p.split_tokens);
     if (t0 >= t1) return;
@@ -324,9 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int t = quarter * 32 + lane;                   // query row in the block = TMEM lane
         const int r = r0 + t;
-        const bool row_ok = r < p.R;
-        const int i = row_ok ? r / p.G : 0;
-        const int hq = h * p.G + (row_ok ? r % p.G : 0);
+        const bool row_in = r < p.R;
+        const int i = row_in ? r / p.G : 0;
+        const int hq = h * p.G + (row_in ? r % p.G : 0);
+        const bool row_ok = row_in && i < nb;                // a padding slot's row is not computed
         const uint64_t anc = row_ok ? anc_s[i] : 0ull;
         const bool warp_rows = __any_sync(0xffffffffu, row_ok);
         const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
@@ -462,8 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tl + kColO + c * 32, o);
                     tmem_wait_ld();
                 }
-                if (!row_ok) continue;
                 const int col0 = c * 32;
+                if (!row_ok) {
+                    if (row_in && !p.merge) {                // padding slot: zeros (the merge writes them otherwise)
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                              ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+                    }
+                    continue;
+                }
                 if (!p.merge) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
                                                           ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);

@@ -10,6 +10,7 @@
 namespace treespec {
 
 constexpr int kMaxNodes = 64;          // one 64-bit ancestry word per node
+constexpr int kAbsent = TREESPEC_ABSENT;   // parent entry of a padding slot past the end of a smaller tree
 constexpr size_t kWsAlign = 256;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -45,7 +46,7 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 
 // Workspace of tree_attn_verify (offsets in bytes from the workspace base).
 struct AttnLayout {
-    size_t status, anc, lens, ml, acc, total;
+    size_t status, anc, lens, nn, ml, acc, total;
 };
 
 struct AttnPlan {
@@ -68,6 +69,7 @@ struct AttnParams {
     uint32_t* status;
     uint64_t* anc;                // [B][N] ancestor-or-self words
     int32_t* lens;                // [B] validated prefix lengths, -1 = invalid sequence
+    int32_t* nn;                  // [B] nodes of each tree: parent entries before the first kAbsent
     float* part_ml;               // [B][Hkv][splits][R][2]  (m in log2 units, l)
     float* part_acc;              // [B][Hkv][splits][R][D]
     int B, N, Hq, Hkv, G, R, D, ps, max_pages, num_pool_pages;

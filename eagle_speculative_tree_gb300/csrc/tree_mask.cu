@@ -4,19 +4,34 @@
 // ancestor of i or j == i; section 5 item 1: with at most 64 nodes the relation is
 // one 64-bit word per node and the test is (word_i >> j) & 1.  The word of node i is
 // its own bit OR the bits of every node on its parent chain.
+//
+// A batch may hold trees of different sizes ("EAGLE-2 & Lookahead Decoding", section 6,
+// batched dynamic tree slicing): a row of the parent array is padded with kAbsent after
+// its tree's N_b nodes.  The prologue records N_b; padding slots get no ancestry bits and
+// the sequence is S + N_b tokens long.
 #include "common.cuh"
 
 namespace treespec {
 
 __global__ void __launch_bounds__(64) tree_prologue_kernel(AttnParams p) {
     __shared__ int par[kMaxNodes];
-    __shared__ int bad;
+    __shared__ int bad, first_pad;
     const int b = blockIdx.x, i = threadIdx.x, N = p.N;
-    if (i == 0) bad = 0;
+    if (i == 0) {
+        bad = 0;
+        first_pad = N;
+    }
     __syncthreads();
+    int pi = 0;
     if (i < N) {
-        int pi = p.parents[(size_t)b * N + i];
-        bool ok = (i == 0) ? (pi == -1) : (pi >= 0 && pi < i);
+        pi = p.parents[(size_t)b * N + i];
+        if (pi == kAbsent) atomicMin(&first_pad, i);
+    }
+    __syncthreads();
+    const int nb = max(first_pad, 1);     // the root is always a node
+    if (i < N) {
+        // a node's parent is an earlier node; every slot after the first padding slot pads too
+        const bool ok = i >= nb ? pi == kAbsent : (i == 0) ? (pi == -1) : (pi >= 0 && pi < i);
         if (!ok) {
             bad = 1;
             pi = (i == 0) ? -1 : 0;       // keep the walk finite: attach to the root
@@ -25,13 +40,17 @@ __global__ void __launch_bounds__(64) tree_prologue_kernel(AttnParams p) {
     }
     __syncthreads();
     if (i < N) {
-        uint64_t w = 1ull << i;
-        for (int j = par[i]; j >= 0; j = par[j]) w |= 1ull << j;   // par[j] < j: at most i steps
+        uint64_t w = 0;
+        if (i < nb) {
+            w = 1ull << i;
+            for (int j = par[i]; j >= 0; j = par[j]) w |= 1ull << j;   // par[j] < j: at most i steps
+        }
         p.anc[(size_t)b * N + i] = w;
     }
     if (i == 0) {
+        p.nn[b] = nb;
         int S = p.prefix_lens[b];
-        long long need = (long long)S + N;
+        long long need = (long long)S + nb;
         bool ok = S >= 0 && need <= (long long)p.max_pages * p.ps;
         p.lens[b] = ok ? S : -1;
         uint32_t st = (bad ? TREESPEC_STATUS_BAD_PARENT : 0u) | (ok ? 0u : TREESPEC_STATUS_BAD_LENGTH);

@@ -31,6 +31,10 @@
  *     with treespec_read_status() after the call.
  *   - Tree layout: tree_parents[b][0] = -1 is the root (the last verified token) and
  *     0 <= tree_parents[b][i] < i for i >= 1 (topological order), N <= 64.
+ *     Trees of different sizes share a batch ("EAGLE-2 & Lookahead Decoding", section
+ *     6, batched dynamic tree slicing): sequence b's tree is the N_b <= N entries
+ *     before the first TREESPEC_ABSENT (-2) of its row, and every later entry must be
+ *     TREESPEC_ABSENT too (a padding slot).
  */
 #ifndef TREESPEC_H
 #define TREESPEC_H
@@ -48,6 +52,9 @@ enum treespec_dtype {
     TREESPEC_DTYPE_F32 = 0,    /* IEEE float32 storage and arithmetic */
     TREESPEC_DTYPE_BF16 = 1,   /* bfloat16 storage, float32 accumulation */
 };
+
+/* Parent entry of a padding slot after a tree smaller than the batch's N. */
+#define TREESPEC_ABSENT (-2)
 
 enum treespec_kernel {
     TREESPEC_KERNEL_AUTO = 0,  /* tensor-core kernel for bf16 with head_dim 128, else CUDA cores */
@@ -77,7 +84,7 @@ enum treespec_error {
 };
 
 enum treespec_status_bits {
-    TREESPEC_STATUS_BAD_PARENT = 1u << 0,  /* parents[0] != -1 or parents[i] not in [0, i) */
+    TREESPEC_STATUS_BAD_PARENT = 1u << 0,  /* parents[0] != -1, parents[i] not in [0, i), or a node after padding */
     TREESPEC_STATUS_BAD_PAGE = 1u << 1,    /* a page id outside [0, num_pool_pages) */
     TREESPEC_STATUS_BAD_LENGTH = 1u << 2,  /* prefix_len < 0 or prefix_len + N > pages * page_size */
     TREESPEC_STATUS_BAD_TOKEN = 1u << 3,   /* a draft token outside [0, vocab) */
@@ -121,8 +128,8 @@ int treespec_attn_plan_for(const treespec_attn_shape *shape, treespec_attn_plan 
  * tree_attn_verify -- one tree-attention verification pass (one layer) for a batch.
  *
  * Operation ("Tech Radar: SGLang EAGLE-2", section 2 mask M and section 5 bitmask):
- * for sequence b with prefix length S = prefix_lens[b], the N tree tokens occupy
- * logical positions S .. S+N-1 in node order.  Logical token t lives in physical
+ * for sequence b with prefix length S = prefix_lens[b], the N_b tree tokens occupy
+ * logical positions S .. S+N_b-1 in node order (N_b = N unless the row is padded).  Logical token t lives in physical
  * page page_table[b][t / page_size], slot t % page_size.  For node i and query head
  * hq (kv head h = hq / G):
  *     allowed(i) = {0 .. S-1} U {S + j : j is an ancestor of i, or j == i}
@@ -130,13 +137,14 @@ int treespec_attn_plan_for(const treespec_attn_shape *shape, treespec_attn_plan 
  *                     applied to V[t][h].
  *
  *   q            [B][N][Hq][D]            dtype
- *   k_pages      [P][page_size][Hkv][D]   dtype  (the tree's own K at positions S..S+N-1)
+ *   k_pages      [P][page_size][Hkv][D]   dtype  (the tree's own K at positions S..S+N_b-1)
  *   v_pages      [P][page_size][Hkv][D]   dtype
- *   page_table   [B][max_pages_per_seq]   int32, entries >= ceil((S+N)/page_size) unused
- *   prefix_lens  [B]                      int32, S >= 0 and S + N <= max_pages_per_seq*page_size
+ *   page_table   [B][max_pages_per_seq]   int32, entries >= ceil((S+N_b)/page_size) unused
+ *   prefix_lens  [B]                      int32, S >= 0 and S + N_b <= max_pages_per_seq*page_size
  *   tree_parents [B][N]                   int32, see the tree layout above
  *   out          [B][N][Hq][D]            dtype, written in full (zeros for a sequence
- *                                         whose prefix length is invalid)
+ *                                         whose prefix length is invalid and for the
+ *                                         rows of padding slots)
  * Slots of a sequence's last page beyond S+N and pages outside the table are never
  * read, so they may hold anything (NaN included).  bf16 outputs are rounded to
  * nearest-even from float32.  All tensors must be 16-byte aligned and contiguous.
@@ -196,7 +204,8 @@ size_t treespec_accept_workspace_bytes(int32_t batch, int32_t num_nodes, int32_t
  *   draft_tokens  [B][N]    int32    token of node i (entry 0, the root, is unused)
  *   draft_probs   [B][N][V] float32  q_i, the draft distribution i's children were drawn
  *                                    from (used as given); may be NULL when T == 0
- *   tree_parents  [B][N]    int32
+ *   tree_parents  [B][N]    int32    may be padded (see the tree layout); a padding
+ *                                    slot's rows and entries are never read as a node
  *   uniforms      [B][N]    float32  uniforms[b][c], c >= 1: accept coin of node c;
  *                                    uniforms[b][0]: the bonus-sample coin; NULL when T == 0
  *   temperature   0 for greedy, else > 0
