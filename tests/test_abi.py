@@ -123,3 +123,14 @@ def test_valid_call_without_device_reports_no_device():
     rc = lib.tree_attn_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(prob.c_shape()),
                               FAKE * 256, 1 << 30, None)
     assert rc == -7
+
+
+def test_padding_sentinel_matches_the_header():
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "treespec.h")).read()
+    m = re.search(r"#define\s+TREESPEC_ABSENT\s+\((-?\d+)\)", hdr)
+    assert m and int(m.group(1)) == ts.ABSENT == -2
+    from gen import trees
+    from oracle.tree_mask import ABSENT
+    assert trees.PAD == ABSENT == ts.ABSENT
