@@ -3,7 +3,9 @@
 // Same partial state as the CUDA-core kernel (m, l, acc per query row of one split),
 // computed with tcgen05:
 //   * one CTA = 128 query rows (row r = node i * G + g of one kv head; padded rows
-//     are zero) x one split of the sequence's logical tokens, in 128-token tiles;
+//     are zero) x one split of the sequence's logical tokens, in 128-token tiles; the
+//     row blocks of one kv head are adjacent in the grid, so they run together and the
+//     second block's K/V reads are served by L2;
 //   * warp 0 streams the split's K pages (four-stage ring) and warp 6 its V pages
 //     (three stages) with TMA (one 16-token page x 64 head-dim columns per copy,
 //     128-byte swizzle; lanes 0-7 issue one page each); the partly filled last page
@@ -69,10 +71,6 @@ struct Bars {
     uint64_t k_full[kNSK], k_empty[kNSK], v_full[kNSV], v_empty[kNSV], s_full[kSB], p_full[kSB], pv_done, q_full, drain;
 };
 
-// CL > 1: the CL CTAs of a cluster hold consecutive row blocks of the same
-// (sequence, kv head, split); each issues the TMA copies of every CL-th page of a tile
-// multicast to all of them, and a stage is refilled only after all CL CTAs released it.
-template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
@@ -118,11 +116,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kNSK; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->k_empty[s], CL);
+            mbar_init(&bars->k_empty[s], 1);
         }
         for (int s = 0; s < kNSV; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->v_empty[s], CL);
+            mbar_init(&bars->v_empty[s], 1);
         }
         for (int s = 0; s < kSB; ++s) {
             mbar_init(&bars->s_full[s], 1);
@@ -142,9 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if constexpr (CL > 1) cluster_sync_all();      // peers' barriers exist before any multicast
-    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
-    constexpr uint16_t kMask = uint16_t((1u << CL) - 1u);
     const uint32_t tbase = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
 
@@ -222,27 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
             if (lane == 0) mbar_arrive_expect_tx(&full[stage], uint32_t(__popc(viatma)) * 2u * 2048u);
             __syncwarp();
-            if (kind == 1 && (CL == 1 || (lane % CL) == int(rank))) {   // each page's two copies
+            if (kind == 1) {                                 // each page's two copies
                 const int z = page * 16;
-                if constexpr (CL == 1) {
-                    tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
-                    tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
-                } else {
-                    tma_load_3d_multicast(dst + lane * 2048, map, 0, h, z, &full[stage], kMask);
-                    tma_load_3d_multicast(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage], kMask);
-                }
+                tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
+                tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
             }
             __syncwarp();
-        }
-        if constexpr (CL > 1) {
-            // every peer's release of every stage has landed here before this CTA may exit
-            for (int s2 = 0; s2 < nst && s2 < ntiles; ++s2) {
-                const int uses = (ntiles - s2 + nst - 1) / nst;
-                if (!mbar_wait_bounded(&empty[s2], (uses - 1) & 1, kWaitNs)) {
-                    *abort_flag = 1;
-                    atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-                }
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -282,8 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
                     mma_bf16_ts(d, tbase + kColQ + kk * 8, kb + koff, kIdS, kk > 0);
                 }
-                if constexpr (CL == 1) mma_commit(&bars->k_empty[stage]);
-                else mma_commit_multicast(&bars->k_empty[stage], kMask);
+                mma_commit(&bars->k_empty[stage]);
                 mma_commit(&bars->s_full[sb]);
             }
             __syncwarp();
@@ -303,8 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBN / 16; ++kk)     // 16 tokens = 8 packed columns of P
                     mma_bf16_ts(tbase + kColO, tbase + kColP + kk * 8, vb + uint64_t((kk * 2048) >> 4), kIdO,
                                 (j > 0 || kk > 0));
-                if constexpr (CL == 1) mma_commit(&bars->v_empty[stage]);
-                else mma_commit_multicast(&bars->v_empty[stage], kMask);
+                mma_commit(&bars->v_empty[stage]);
                 mma_commit(&bars->pv_done);
             }
             __syncwarp();
@@ -507,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, kTmemCols);
-    if constexpr (CL > 1) cluster_sync_all();      // no peer still writes into this CTA
 }
 
 }  // namespace
@@ -543,44 +520,15 @@ bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_t
 
 bool attn_tc_supported(int dtype, int D) { return dtype == TREESPEC_DTYPE_BF16 && D == kD; }
 
-template <int CL>
-cudaError_t launch_cluster(const AttnParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s) {
-    auto kern = attn_tc_kernel<CL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_splits, p.Hkv * p.row_blocks, p.B);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = CL;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = CL > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
-// Pairs of row blocks of one kv head share each K/V copy (multicast): half the L2 reads
-// and TMA copies per CTA.  Clusters of 4 fit only 144 of the 152 SMs (whole GPCs),
-// clusters of 2 all of them.  Measured on 32 x 8192-token sequences (64 q / 8 kv heads,
-// 64 tree nodes): 0.532 ms without clusters, 0.493 ms with pairs, 0.60 ms with 4.
-int attn_tc_cluster_size(int row_blocks) { return row_blocks % 2 == 0 ? 2 : 1; }
-
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s) {
     CUtensorMap mk, mv;
     const long long pool_tokens = (long long)p.num_pool_pages * p.ps;
     if (!make_pool_map(&mk, p.k, p.Hkv, pool_tokens) || !make_pool_map(&mv, p.v, p.Hkv, pool_tokens))
         return cudaErrorInvalidValue;
-    switch (attn_tc_cluster_size(p.row_blocks)) {
-        case 4: return launch_cluster<4>(p, mk, mv, s);
-        case 2: return launch_cluster<2>(p, mk, mv, s);
-        default: return launch_cluster<1>(p, mk, mv, s);
-    }
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_tc_kernel<<<dim3(p.num_splits, p.Hkv * p.row_blocks, p.B), kThreads, kSmemBytes, s>>>(p, mk, mv);
+    return cudaGetLastError();
 }
 
 }  // namespace treespec

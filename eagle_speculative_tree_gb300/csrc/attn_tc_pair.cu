@@ -76,11 +76,6 @@ constexpr int kOffAnc = kOffMisc + 16;
 constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;         // 230,208 bytes
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// CL > 1: the CL CTAs of a cluster hold consecutive row-block pairs of the same
-// (sequence, kv head, split); each issues the TMA copies of every CL-th page of a tile
-// multicast to all of them, and a stage is refilled only after both tiles of all CL
-// CTAs released it.
-template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_pair_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv) {
@@ -125,11 +120,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kNSK; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->k_empty[s], kNQ * CL);
+            mbar_init(&bars->k_empty[s], kNQ);
         }
         for (int s = 0; s < kNSV; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->v_empty[s], kNQ * CL);
+            mbar_init(&bars->v_empty[s], kNQ);
         }
         for (int t = 0; t < kNQ; ++t) {
             mbar_init(&bars->q_full[t], kM);
@@ -152,9 +147,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if constexpr (CL > 1) cluster_sync_all();      // peers' barriers exist before any multicast
-    const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
-    constexpr uint16_t kMask = uint16_t((1u << CL) - 1u);
     const uint32_t tbase = *tmem_slot;
     const uint32_t sbase = smem_u32(sm);
     if (warp >= kWarpK) {
@@ -230,27 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
             if (lane == 0) mbar_arrive_expect_tx(&full[stage], uint32_t(__popc(viatma)) * 2u * 2048u);
             __syncwarp();
-            if (kind == 1 && (CL == 1 || (lane % CL) == int(rank))) {   // each page's two copies
+            if (kind == 1) {                                 // each page's two copies
                 const int z = page * 16;
-                if constexpr (CL == 1) {
-                    tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
-                    tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
-                } else {
-                    tma_load_3d_multicast(dst + lane * 2048, map, 0, h, z, &full[stage], kMask);
-                    tma_load_3d_multicast(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage], kMask);
-                }
+                tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
+                tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
             }
             __syncwarp();
-        }
-        if constexpr (CL > 1) {
-            // every peer's release of every stage has landed here before this CTA may exit
-            for (int s2 = 0; s2 < nst && s2 < ntiles; ++s2) {
-                const int uses = (ntiles - s2 + nst - 1) / nst;
-                if (!mbar_wait_bounded(&empty[s2], (uses - 1) & 1, kWaitNs)) {
-                    *abort_flag = 1;
-                    atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-                }
-            }
         }
       } else {
         // ------------------------------------------------------------ MMA issuers
@@ -290,8 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t koff = uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
                         mma_bf16_ss(dS + bf * 64u, dq + qoff, kb + koff, kIdS, kk > 0);
                     }
-                    if constexpr (CL == 1) mma_commit(&bars->k_empty[ks]);
-                    else mma_commit_multicast(&bars->k_empty[ks], kMask);
+                    mma_commit(&bars->k_empty[ks]);
                     mma_commit(&bars->s_full[t][bf]);
                 }
                 __syncwarp();
@@ -308,8 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBN / 16; ++kk)     // 16 tokens = 8 packed columns of P
                         mma_bf16_ts(dO, dS + bf * 64u + kk * 8, vb + uint64_t((kk * 2048) >> 4), kIdO,
                                     (jp > 0 || kk > 0));
-                    if constexpr (CL == 1) mma_commit(&bars->v_empty[vs]);
-                    else mma_commit_multicast(&bars->v_empty[vs], kMask);
+                    mma_commit(&bars->v_empty[vs]);
                     mma_commit(&bars->pv_done[t][bf]);
                     if (jp == ntiles - 1) mma_commit(&bars->o_full[t]);
                 }
@@ -505,36 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpMma) tmem_dealloc(tbase, kTmemCols);
-    if constexpr (CL > 1) cluster_sync_all();      // no peer still writes into this CTA
-}
-
-template <int CL>
-cudaError_t launch_pair_cluster(const AttnParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t s) {
-    auto kern = attn_tc_pair_kernel<CL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_splits, p.Hkv * (p.row_blocks / kNQ), p.B);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = CL;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = CL > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
 }
 
 }  // namespace
-
-// Pairs of CTAs of one kv head (four row blocks) share each K/V copy when the head has
-// an even number of row-block pairs.
-int attn_tc_pair_cluster_size(int row_blocks) { return (row_blocks / kNQ) % 2 == 0 ? 2 : 1; }
 
 cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s) {
     if (p.row_blocks % kNQ != 0 || p.rows_per_block != kM) return cudaErrorInvalidValue;
@@ -542,8 +490,12 @@ cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s) {
     const long long pool_tokens = (long long)p.num_pool_pages * p.ps;
     if (!make_pool_map(&mk, p.k, p.Hkv, pool_tokens) || !make_pool_map(&mv, p.v, p.Hkv, pool_tokens))
         return cudaErrorInvalidValue;
-    if (attn_tc_pair_cluster_size(p.row_blocks) == 2) return launch_pair_cluster<2>(p, mk, mv, s);
-    return launch_pair_cluster<1>(p, mk, mv, s);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attn_tc_pair_kernel<<<dim3(p.num_splits, p.Hkv * (p.row_blocks / kNQ), p.B), kThreads, kSmemBytes, s>>>(p, mk,
+                                                                                                          mv);
+    return cudaGetLastError();
 }
 
 }  // namespace treespec

@@ -107,8 +107,6 @@ cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s);
 bool attn_tc_supported(int dtype, int D);
-int attn_tc_cluster_size(int row_blocks);
-int attn_tc_pair_cluster_size(int row_blocks);
 // TMA map of a K or V page pool [P][16][Hkv][128] bf16, one page x 64 head dims per box
 bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_tokens);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
