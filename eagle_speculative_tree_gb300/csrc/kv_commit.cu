@@ -1,7 +1,8 @@
 // tree_kv_commit: move the accepted path's K/V rows next to the prefix, in place.
 //
-// One CTA per (sequence, kv head).  Thread 0 checks the sequence's prefix length and
-// path; every thread checks the page ids of the rows it moves.  The CTA then reads all
+// One CTA per (sequence, kv head).  Thread 0 checks the sequence's path and that every
+// position the commit touches (S .. S + max(path)) lies in its page table; every thread
+// checks the page ids of the rows it moves.  The CTA then reads all
 // source rows of K into shared memory, waits, writes them to their destinations, and
 // does the same for V -- so a destination that is also a later source is never
 // overwritten before it is read.  Rows move as 16-byte words.
@@ -23,7 +24,7 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(const CommitP
     if (tid == 0) {
         const int S = p.prefix_lens[b], n = p.len[b];
         uint32_t bad = 0;
-        if (S < 0 || (long long)S + p.N > (long long)p.max_pages * p.ps) bad |= TREESPEC_STATUS_BAD_LENGTH;
+        int top = 0;                                     // deepest node moved: positions S .. S + top are touched
         if (n < 0 || n > p.N - 1) {
             bad |= TREESPEC_STATUS_BAD_PATH;
         } else {
@@ -33,7 +34,11 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(const CommitP
                 if (x <= prev || x >= p.N) { bad |= TREESPEC_STATUS_BAD_PATH; break; }
                 prev = x;
             }
+            if (!bad) top = prev;
         }
+        // the bound is what the moves touch, not the tree size: a tree padded after its own
+        // last node commits whenever its accepted path fits the page table
+        if (S < 0 || (long long)S + 1 + top > (long long)p.max_pages * p.ps) bad |= TREESPEC_STATUS_BAD_LENGTH;
         s_ok = bad == 0;
         s_len = bad ? 0 : n;
         s_S = S;

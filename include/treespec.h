@@ -172,12 +172,21 @@ int tree_attn_verify(const void *q, const void *k_pages, const void *v_pages,
  *     argument errors are those of tree_attn_verify.
  *   - All calls on a device share the array: calls whose work overlaps on the GPU race
  *     and corrupt each other; serialise them (one stream).  The device status word of
- *     these calls is not exposed -- use tree_attn_verify to read it.
+ *     the last call is read with treespec_noalloc_read_status.
  */
 int tree_attn_verify_noalloc(const void *q, const void *k_pages, const void *v_pages,
                              const int32_t *page_table, const int32_t *prefix_lens,
                              const int32_t *tree_parents, void *out,
                              const treespec_attn_shape *shape, treespec_stream_t stream);
+
+/*
+ * treespec_noalloc_read_status -- synchronise `stream` and copy the device status word
+ * (TREESPEC_STATUS_* bits) of the last tree_attn_verify_noalloc call on the current
+ * device into *status.  Like the entry point it serves, the method's description has no
+ * counterpart to it: a caller of the no-allocation entry point holds no workspace
+ * pointer, so treespec_read_status cannot reach its status word.  Returns an error code.
+ */
+int treespec_noalloc_read_status(uint32_t *status, treespec_stream_t stream);
 
 /* --------------------------------------------------------------------- accept walk */
 
@@ -264,10 +273,15 @@ size_t treespec_commit_workspace_bytes(void);
  *   new_prefix_lens [B]                          int32 out (a separate buffer)
  *   shape: batch, num_nodes, num_kv_heads, head_dim, page_size, max_pages_per_seq,
  *          num_pool_pages and dtype are used; num_q_heads, kernel, num_splits are not.
- * A sequence whose prefix length is invalid (BAD_LENGTH), whose accept_len is outside
- * [0, N-1] or whose path does not increase strictly within [1, N) (BAD_PATH), or whose
- * pages touched are outside the pool (BAD_PAGE) is left unchanged and gets
- * new_prefix_lens[b] = -1; the bit goes to the workspace status word.
+ * The commit touches logical positions S .. S + max(path) only (the root stays at S), so
+ * the bound is S + 1 + max(path) <= max_pages_per_seq * page_size (max(path) = 0 for an
+ * empty path), whatever N is: a tree padded after its own last node with TREESPEC_ABSENT
+ * commits whenever its accepted path fits.
+ * A sequence whose prefix length is negative or whose touched positions run past its
+ * page table (BAD_LENGTH), whose accept_len is outside [0, N-1] or whose path does not
+ * increase strictly within [1, N) (BAD_PATH), or whose pages touched are outside the pool
+ * (BAD_PAGE) is left unchanged and gets new_prefix_lens[b] = -1; the bit goes to the
+ * workspace status word.
  */
 int tree_kv_commit(void *k_pages, void *v_pages, const int32_t *page_table,
                    const int32_t *prefix_lens, const int32_t *accept_path,

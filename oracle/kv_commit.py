@@ -11,6 +11,13 @@ accepted path means the sequence becomes the prefix, the root, and the accepted 
 path order -- node path[k] moves to position S + 1 + k -- and its length S + 1 + len;
 everything after that is free.  All values are copied exactly (no arithmetic).
 
+The positions a commit touches are S (the root, which stays) through S + max(path) (the
+deepest source; every destination S + 1 + k lies at or before it because a strictly
+increasing path from 1 has path[k] >= k + 1).  Those positions must lie in the page
+table: S + 1 + max(path) <= pages * page_size, with max(path) = 0 for an empty path.  The
+tree's node count does not enter the bound, so a tree smaller than the batch's N (a row
+padded after its last node) commits whenever its own accepted path fits.
+
 A sequence whose prefix length, path or pages are invalid is left untouched and reports
 new length -1 with a status flag, as the CUDA entry point does.
 """
@@ -32,12 +39,13 @@ def kv_commit(k_pages: np.ndarray, v_pages: np.ndarray, page_table: np.ndarray, 
     for b in range(B):
         S, n = int(prefix_lens[b]), int(accept_len[b])
         bad = 0
-        if S < 0 or S + num_nodes > max_pages * ps:
-            bad |= BAD_LENGTH
         path = [int(x) for x in accept_path[b, :max(n, 0)]] if 0 <= n <= num_nodes - 1 else None
         if path is None or any(x >= num_nodes for x in path) or any(
                 x <= prev for prev, x in zip([0] + path[:-1], path)):
             bad |= BAD_PATH
+        top = path[-1] if (not bad and path) else 0              # deepest position touched: S + top
+        if S < 0 or S + 1 + top > max_pages * ps:
+            bad |= BAD_LENGTH
         if bad:
             status |= bad
             continue

@@ -104,3 +104,27 @@ def test_commit_rejects_bad_inputs_without_moving(ts, cuda_device):
     pt[3, (pl[3] + 1) // 16] = x.num_pool_pages + 7   # a destination page outside the pool
     st, want = run_both(ts, x, cuda_device, path, lens, prefix_lens=pl, page_table=pt)
     assert st == want and st & okc.BAD_PATH and st & okc.BAD_LENGTH and st & okc.BAD_PAGE
+
+
+def test_commit_of_a_padded_tree_near_the_end_of_its_pages(ts, cuda_device):
+    """A 5-node tree padded to the batch's 64 nodes, its prefix placed so that S + 64 runs
+    past its page table while S + 5 fits: the accepted path commits (bound S + 1 +
+    max(path)), bit-exact against the oracle, beside a full 64-node tree."""
+    from dataclasses import replace
+    rng = np.random.default_rng(11)
+    w = replace(gen.get("c2_llama3_8b_bf16_greedy").with_batch(2), num_nodes=64)
+    parents = trees.padded([trees.random_recursive(rng, 64), trees.chain(5)], 64)
+    prefix = np.array([100, 170], dtype=np.int32)
+    x = gi.make_inputs(w, parents=parents, prefix_lens=prefix, with_accept=False)
+    table = np.ascontiguousarray(x.page_table[:, :11])       # 176 slots: 100 + 64 and 170 + 5 fit, 170 + 64 not
+    path = np.full((2, 64), -1, dtype=np.int32)
+    lens = np.zeros(2, dtype=np.int32)
+    p0 = trees.random_root_path(parents[0], rng, 0.0)
+    path[0, :len(p0)], lens[0] = p0, len(p0)
+    path[1, :4], lens[1] = [1, 2, 3, 4], 4                    # touches positions 170 .. 174
+    st, want = run_both(ts, x, cuda_device, path, lens, page_table=table)
+    assert st == 0 and want == 0
+    prefix2 = prefix.copy()
+    prefix2[1] = 172                                          # now node 4 would sit at 176: past the table
+    st, want = run_both(ts, x, cuda_device, path, lens, prefix_lens=prefix2, page_table=table)
+    assert st == want and st & okc.BAD_LENGTH

@@ -90,7 +90,8 @@ def test_sequence_becomes_prefix_root_and_path(seed):
 
 @pytest.mark.parametrize("S,path,n,bit", [
     (-1, [1], 1, okc.BAD_LENGTH),            # negative prefix
-    (60, [1], 1, okc.BAD_LENGTH),            # tree runs past the page table (64 slots, N = 8)
+    (62, [2], 1, okc.BAD_LENGTH),            # the source at 62 + 2 lies past the page table (64 slots)
+    (64, [], 0, okc.BAD_LENGTH),             # even the root lies past it
     (0, [2, 2], 2, okc.BAD_PATH),            # not strictly increasing
     (0, [0], 1, okc.BAD_PATH),               # the root is not a path entry
     (0, [9], 1, okc.BAD_PATH),               # node index >= N
@@ -110,3 +111,36 @@ def test_bad_page_is_reported_and_nothing_moves():
     k2, _v, lens, st = okc.kv_commit(k, -k, np.array([[0, 9, 2, 3]], dtype=np.int32), np.array([14]),
                                       np.array([[2, -1, -1, -1, -1, -1, -1, -1]]), np.array([1]), num_nodes=8)
     assert st & okc.BAD_PAGE and lens.tolist() == [-1] and np.array_equal(k2, k)
+
+
+def test_bound_is_the_deepest_position_touched_not_the_tree_size():
+    # A tree of N = 8 nodes at S = 60 would run past 64 slots, but a commit only touches
+    # positions S .. S + max(path): path [1, 3] touches 60..63 and fits; path [1, 4] reaches
+    # position 64 and does not.  An empty path touches only the root.
+    k = tagged_pool(4)
+    pt = np.array([[0, 1, 2, 3]], dtype=np.int32)
+    for path, n, ok in [([1, 3], 2, True), ([1, 4], 2, False), ([], 0, True), ([3], 1, True)]:
+        pth = np.full((1, 8), -1)
+        pth[0, :len(path)] = path
+        k2, _v, lens, st = okc.kv_commit(k, -k, pt, np.array([60]), pth, np.array([n]), num_nodes=8)
+        if ok:
+            assert st == 0 and lens.tolist() == [61 + n]
+            for j, x in enumerate(path):          # node x (position 60 + x) now sits at 61 + j
+                src, dst = 60 + x, 61 + j
+                assert np.array_equal(k2[pt[0, dst // PS], dst % PS], k[pt[0, src // PS], src % PS])
+        else:
+            assert st & okc.BAD_LENGTH and lens.tolist() == [-1] and np.array_equal(k2, k)
+
+
+def test_padded_tree_commits_like_the_same_tree_unpadded():
+    # the same 5-node tree, once alone (N = 5) and once padded to N = 12 with absent slots:
+    # the committed pools and lengths agree, also where S + 12 exceeds the page table
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((4, PS, 2, 4))
+    pt = np.array([[2, 0, 3, 1]], dtype=np.int32)
+    path = np.array([[1, 4] + [-1] * 10])
+    for S in (10, 57, 59):
+        a = okc.kv_commit(k, -k, pt, np.array([S]), path[:, :5], np.array([2]), num_nodes=5)
+        b = okc.kv_commit(k, -k, pt, np.array([S]), path, np.array([2]), num_nodes=12)
+        assert a[3] == b[3] == 0 and a[2].tolist() == b[2].tolist() == [S + 3]
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
