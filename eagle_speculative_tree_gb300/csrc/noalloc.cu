@@ -71,3 +71,19 @@ extern "C" int tree_attn_verify_noalloc(const void* q, const void* k_pages, cons
     return tree_attn_verify(q, k_pages, v_pages, page_table, prefix_lens, tree_parents, out, shape, scratch,
                             kScratchBytes, stream);
 }
+
+// The device status word of the last tree_attn_verify_noalloc call on the current device
+// (the first word of the fixed array, where the workspace layout keeps it).  Waits for
+// `stream` first.  Callers of the no-allocation entry point have no workspace pointer
+// to hand treespec_read_status, so this is their only view of the bad-index and
+// timeout bits the kernels set.
+extern "C" int treespec_noalloc_read_status(uint32_t* status, treespec_stream_t stream) {
+    if (!status) return TREESPEC_ERR_NULL_POINTER;
+    void* scratch = nullptr;
+    const int rc = scratch_of_current_device(&scratch);
+    if (rc != TREESPEC_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (cudaMemcpy(status, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TREESPEC_ERR_LAUNCH;
+    return TREESPEC_OK;
+}

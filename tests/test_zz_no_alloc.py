@@ -29,7 +29,16 @@ def ts():
     lib = mod.raw_library()
     lib.tree_attn_verify_noalloc.argtypes = [ctypes.c_void_p] * 7 + [ctypes.POINTER(mod.AttnShape), ctypes.c_void_p]
     lib.tree_attn_verify_noalloc.restype = ctypes.c_int
+    lib.treespec_noalloc_read_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
+    lib.treespec_noalloc_read_status.restype = ctypes.c_int
     return mod
+
+
+def _noalloc_status(ts):
+    st = ctypes.c_uint32(0)
+    assert ts.raw_library().treespec_noalloc_read_status(ctypes.byref(st),
+                                                          torch.cuda.current_stream().cuda_stream) == 0
+    return st.value
 
 
 def _noalloc(ts, d, out, prob):
@@ -74,3 +83,40 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(ts, cuda_device):
     bad = ts.attn_problem(d["q"], d["k_pages"], d["page_table"])
     bad.num_nodes = 65
     assert _noalloc(ts, d, out, bad) == -2
+
+
+def test_noalloc_padded_trees_back_to_back(ts, cuda_device):
+    """Trees of different sizes (rows padded with -2), two calls in a row with different
+    padding: the second call reuses the array's node counts and ancestor words the first
+    one left, and must still match the workspace entry point."""
+    from gen import trees
+    w = gen.get("c4_llama3_70b_bf16_greedy").with_batch(4)
+    rng = np.random.default_rng(21)
+    for sizes in ([64, 17, 1, 40], [9, 64, 33, 2]):
+        parents = trees.padded([trees.random_recursive(rng, n) for n in sizes], w.num_nodes)
+        x = gi.make_inputs(w, parents=parents, prefix_lens=np.asarray([100, 37, 0, 300], dtype=np.int32),
+                           with_accept=False)
+        d = attn_device_inputs(x, cuda_device)
+        ref = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"],
+                                  d["tree_parents"])
+        out = torch.full_like(d["q"], float("nan"))
+        assert _noalloc(ts, d, out, ts.attn_problem(d["q"], d["k_pages"], d["page_table"])) == 0
+        assert _noalloc_status(ts) == 0
+        _close(out, ref, w.dtype)
+        for b, n in enumerate(sizes):
+            assert torch.all(out[b, n:] == 0)
+
+
+def test_noalloc_status_word_flags_a_bad_page_then_clears(ts, cuda_device):
+    w = gen.get("c2_llama3_8b_bf16_greedy")
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    prob = ts.attn_problem(d["q"], d["k_pages"], d["page_table"])
+    good = d["page_table"].clone()
+    d["page_table"][0, 2] = 1 << 30
+    out = torch.zeros_like(d["q"])
+    assert _noalloc(ts, d, out, prob) == 0
+    assert _noalloc_status(ts) & 2                     # TREESPEC_STATUS_BAD_PAGE
+    d["page_table"] = good
+    assert _noalloc(ts, d, out, prob) == 0
+    assert _noalloc_status(ts) == 0
