@@ -60,6 +60,31 @@ def algorithmic_work(x: gi.TreeInputs):
     return dict(kv_bytes=kv_bytes, attn_bytes=attn_bytes, attn_flops=attn_flops, accept_bytes=accept_bytes)
 
 
+# Every configuration the metric is quoted per (batch x prefix x tree): the five workloads,
+# with the Llama-3-70B shape at batches 1, 8 and 32, greedy and at T = 0.7.
+SWEEP = ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy", "c3_llama2_7b_bf16_stoch",
+         "c4_llama3_70b_bf16_greedy@b1", "c4_llama3_70b_bf16_t0.7@b1",
+         "c4_llama3_70b_bf16_greedy@b8", "c4_llama3_70b_bf16_t0.7@b8",
+         "c4_llama3_70b_bf16_greedy", "c4_llama3_70b_bf16_t0.7", "c5_ragged_b64_bf16_stoch"]
+KERNEL_NAMES = {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_tc_pair_kernel"}
+L2_FLUSH_BYTES = 512 << 20       # written before every timed call of the sweep: 4x the 129 MB L2
+
+
+def attn_roofline(work, t_attn_ms, hbm, tf_burst):
+    """Achieved rates of one tree_attn_verify and the roof that binds it.  The tensor roof is
+    the burst bf16 peak: every timed region here is milliseconds long, at full clock."""
+    t = t_attn_ms * 1e-3
+    tflops = work["attn_flops"] / t / 1e12
+    gbs = work["attn_bytes"] / t / 1e9
+    t_tc = work["attn_flops"] / (tf_burst * 1e12)
+    t_hbm = work["attn_bytes"] / (hbm * 1e9)
+    bound = "tensor" if t_tc > t_hbm else "hbm"
+    return dict(bound=bound, tflops=tflops, gbs=gbs, tensor_frac=tflops / tf_burst, hbm_frac=gbs / hbm,
+                frac=(tflops / tf_burst) if bound == "tensor" else (gbs / hbm),
+                # the largest fraction of HBM the KV reads can reach when the tensor pipe runs at its peak
+                kv_frac_cap=min(1.0, work["kv_bytes"] / max(t_tc, t_hbm) / 1e9 / hbm))
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "eagle_speculative_tree_gb300", "csrc")
@@ -151,6 +176,92 @@ def job_throughput(world: int, steps: int, local_ms: float, device) -> tuple:
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = float(tt.item())
     return t, world * steps / (t * 1e-3)
+
+
+def to_device(x: gi.TreeInputs, dev):
+    import torch
+    w = x.workload
+    bf = w.dtype == "bf16"
+
+    def t(a, bf16=False):
+        a = np.ascontiguousarray(a)
+        h = torch.from_numpy(a.view(np.int16) if bf16 else a).to(dev)
+        return h.view(torch.bfloat16) if bf16 else h
+
+    return dict(q=t(x.q, bf), k=t(x.k_pages, bf), v=t(x.v_pages, bf), pt=t(x.page_table), pl=t(x.prefix_lens),
+                par=t(x.tree_parents), lg=t(x.target_logits), tok=t(x.draft_tokens),
+                qp=None if w.greedy else t(x.draft_probs), u=None if w.greedy else t(x.uniforms))
+
+
+def sweep_one(ts, name, dev, stream, steps, warmup, flush, hbm, tf_burst):
+    """One configuration: `steps` timed tree_attn_verify + tree_accept pairs, each call timed
+    by its own CUDA events with L2 flushed (a 512 MB write) before it."""
+    import torch
+    w = gen.get(name)
+    x = gi.make_inputs(w)
+    d = to_device(x, dev)
+    out = torch.empty_like(d["q"])
+    prob = ts.attn_problem(d["q"], d["k"], d["pt"])
+    plan = ts.attn_plan(prob)
+    ws_a = torch.empty(ts.attn_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(ts.accept_workspace_bytes(w.batch, w.num_nodes, w.vocab), dtype=torch.uint8, device=dev)
+    path = torch.empty((w.batch, w.num_nodes), dtype=torch.int32, device=dev)
+    alen = torch.empty((w.batch,), dtype=torch.int32, device=dev)
+    bonus = torch.empty((w.batch,), dtype=torch.int32, device=dev)
+
+    def attn():
+        ts.tree_attn_verify(d["q"], d["k"], d["v"], d["pt"], d["pl"], d["par"], out, workspace=ws_a, stream=stream)
+
+    def acc():
+        ts.tree_accept(d["lg"], d["tok"], d["qp"], d["par"], d["u"], w.temperature, accept_path=path,
+                       accept_len=alen, bonus_token=bonus, workspace=ws_b, stream=stream)
+
+    for _ in range(warmup):
+        attn()
+        acc()
+    torch.cuda.synchronize()
+    if ts.read_status(ws_a) or ts.read_status(ws_b):
+        raise RuntimeError(f"{name}: device status flagged an input error")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        attn()
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        acc()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    ta = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    tb = np.array([e[2].elapsed_time(e[3]) for e in ev])
+    work = algorithmic_work(x)
+    t_attn, t_acc = float(ta.mean()), float(tb.mean())
+    roof = attn_roofline(work, t_attn, hbm, tf_burst)
+    kv_gbs = work["kv_bytes"] / (t_attn * 1e-3) / 1e9
+    lens = alen.cpu().numpy()
+    return {"workload": w.name, "batch": w.batch, "tree_nodes": w.num_nodes, "temperature": w.temperature,
+            "plan": {"kernel": KERNEL_NAMES[plan.kernel], "num_splits": plan.num_splits, "merge": bool(plan.merge)},
+            "t_attn_ms": round(t_attn, 4), "t_attn_p10_p90_ms": [round(float(np.percentile(ta, 10)), 4),
+                                                               round(float(np.percentile(ta, 90)), 4)],
+            "t_accept_ms": round(t_acc, 4), "steps_per_s": round(1e3 / (t_attn + t_acc), 1),
+            "kv_read_gbs": round(kv_gbs, 1), "kv_frac_of_hbm_peak": round(kv_gbs / hbm, 4),
+            "attn_tflops": round(roof["tflops"], 1), "tensor_frac": round(roof["tensor_frac"], 4),
+            "bound": roof["bound"], "frac": round(roof["frac"], 4), "kv_frac_cap": round(roof["kv_frac_cap"], 4),
+            "mean_accept_len": round(float(lens.mean()), 3)}
+
+
+def run_sweep(ts, dev, stream, steps, warmup):
+    import torch
+    hbm, tf_burst, _tf_sus, _src = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    rows = []
+    for name in SWEEP:
+        rows.append(sweep_one(ts, name, dev, stream, steps, warmup, flush, hbm, tf_burst))
+        torch.cuda.empty_cache()
+    return {"note": "each call timed alone by CUDA events with L2 flushed before it; steps_per_s = "
+                    "1 / (t_attn + t_accept); frac = fraction of the binding roof (burst bf16 tensor peak "
+                    "or HBM copy rate, measured)", "steps": steps, "configs": rows}
 
 
 def run_gpu(args):
@@ -383,21 +494,21 @@ def run_gpu(args):
     work = algorithmic_work(x)
     hbm, tf_burst, tf_sus, src = peaks()
     kv_gbs = work["kv_bytes"] / (t_attn * 1e-3) / 1e9
-    attn_gbs = work["attn_bytes"] / (t_attn * 1e-3) / 1e9
-    attn_tflops = work["attn_flops"] / (t_attn * 1e-3) / 1e12
-    t_hbm = work["attn_bytes"] / (hbm * 1e9)
-    t_tc = work["attn_flops"] / (tf_sus * 1e12)
-    kernel_name = {1: "attn_simt_kernel", 2: "attn_tc_kernel", 3: "attn_tc_pair_kernel"}[plan.kernel]
+    kernel_name = KERNEL_NAMES[plan.kernel]
     traffic = recorded_traffic(w.name, kernel_name)
-    if t_tc > t_hbm:
-        roof = {"bound": "tensor", "achieved": round(attn_tflops, 2), "peak": tf_sus, "unit": "TFLOP/s",
-                "frac": round(attn_tflops / tf_sus, 4), "traffic": traffic}
+    rf = attn_roofline(work, t_attn, hbm, tf_burst)
+    if rf["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": round(rf["tflops"], 2), "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": round(rf["frac"], 4), "traffic": traffic, "peak_kind": "burst bf16 (of " + src + ")"}
     else:
-        roof = {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(attn_gbs / hbm, 4), "traffic": traffic}
+        roof = {"bound": "hbm", "achieved": round(rf["gbs"], 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(rf["frac"], 4), "traffic": traffic, "peak_kind": "HBM copy (of " + src + ")"}
     roof.update({"kernel": f"tree_attn_verify ({kernel_name} + prologue" + (" + merge)" if plan.merge else ")"),
-                 "peak_source": src, "algorithmic_bytes": work["attn_bytes"], "algorithmic_flops": work["attn_flops"],
-                 "launch_ms": round(t_attn, 4)})
+                 "algorithmic_bytes": work["attn_bytes"], "algorithmic_flops": work["attn_flops"],
+                 "launch_ms": round(t_attn, 4), "hbm_frac": round(rf["hbm_frac"], 4),
+                 "tensor_frac": round(rf["tensor_frac"], 4), "kv_frac_cap": round(rf["kv_frac_cap"], 4),
+                 "kv_frac_cap_note": "KV bytes / max(FLOPs / burst tensor peak, bytes / HBM peak) / HBM peak: "
+                                     "the KV fraction this workload can reach with the tensor pipe at its peak"})
     ms_step = total_ms / K
     lens = alen.cpu().numpy()
     line = {
@@ -412,6 +523,7 @@ def run_gpu(args):
                    "l2": f"inputs larger than L2 (KV {work['kv_bytes'] / 1e9:.2f} GB, accept rows "
                          f"{work['accept_bytes'] / 1e9:.2f} GB per step)"},
         "kv_read_gbs": round(kv_gbs, 1), "kv_frac_of_hbm_peak": round(kv_gbs / hbm, 4),
+        "kv_frac_cap": round(rf["kv_frac_cap"], 4),
         "t_attn_ms": round(t_attn, 4), "t_accept_ms": round(ms_step - t_attn, 4),
         "attn_plan": {"kernel": kernel_name, "num_splits": plan.num_splits, "split_tokens": plan.split_tokens,
                       "merge": bool(plan.merge)},
@@ -434,6 +546,10 @@ def run_gpu(args):
                        "note": "tree_draft_step x steps + tree_rerank for the next tree, timed apart from the step"},
         "clocks": clk,
     }
+    if world == 1 and not args.no_sweep:
+        del d, resident, host, rows_h, dsts, outs, hres
+        torch.cuda.empty_cache()
+        line["sweep"] = run_sweep(ts, dev, stream, min(K, 20), args.warmup)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if rank == 0:
@@ -478,6 +594,8 @@ class OracleSample:
         t_acc_full = t_acc * w.batch / self.sample_b
         t_step = t_attn_full + t_acc_full
         return {"value": round(1.0 / t_step, 6), "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+                "estimate": "scaled: the sample's measured time x (full step's tokens / sample's tokens); "
+                            "the full step itself is not run",
                 "sample": f"float64 oracle: attention over {len(done)} (sequence, kv head) pairs and the accept "
                           f"walk over {self.sample_b} sequences, scaled by tokens to the full {w.name} step",
                 "t_attn_s_full_step": round(t_attn_full, 3), "t_accept_s_full_step": round(t_acc_full, 3)}
@@ -525,6 +643,7 @@ def main():
     ap.add_argument("--attn-kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--accept-mode", type=int, default=0, help="0 auto, 1 all rows, 2 path only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep (1 GPU only)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     args = ap.parse_args()
     if args.warmup < 3:
