@@ -11,6 +11,7 @@ namespace treespec {
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};     // see treespec_set_wait_limit_ns
 
 constexpr int kDefaultSms = 152;
 constexpr int kMaxDevices = 64;
@@ -81,14 +82,13 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
                        (long long)s.num_pool_pages * s.page_size < (1ll << 31);
     // Tensor cores for every bf16 / head_dim 128 shape: measured faster than the CUDA-core
     // kernel from 16 rows per kv head up (rows are padded to the 128-row MMA tile).
-    // The two-tile kernel only where it measured faster: its CTAs (one per pair of row
-    // blocks) fill the SMs in one wave while the one-tile kernel's would need two (32 x
-    // 8192 tokens, 64 q / 8 kv heads, 64 nodes: 0.129 ms against 0.134 at batch 8, 0.471
-    // against 0.441 at batch 32).
+    // The two-tile kernel wherever the row blocks of a kv head pair up: one CTA then reads
+    // each K/V tile for 256 query rows, the one-tile kernel for 128, and the L2 reads of the
+    // one-tile kernel bind first (32 x 8192 tokens, 64 q / 8 kv heads, 64 nodes: 0.471 ms
+    // against 0.541 at batch 32, 0.244 against 0.317 at batch 16).
     if (s.kernel == TREESPEC_KERNEL_TC || s.kernel == TREESPEC_KERNEL_TC_PAIR ||
         (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
-        const long long blocks = (long long)s.batch * s.num_kv_heads * ((R + 127) / 128);
-        const bool paired = ((R + 127) / 128) % 2 == 0 && blocks / 2 <= sms && blocks > sms;
+        const bool paired = ((R + 127) / 128) % 2 == 0;
         p.kernel = s.kernel == TREESPEC_KERNEL_TC ? TREESPEC_KERNEL_TC
                    : (s.kernel == TREESPEC_KERNEL_TC_PAIR || paired) ? TREESPEC_KERNEL_TC_PAIR
                                                                       : TREESPEC_KERNEL_TC;
@@ -256,6 +256,7 @@ extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* 
     p.row_blocks = plan.row_blocks;
     p.merge = plan.merge;
     p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(s.head_dim)));
+    p.wait_ns = g_wait_ns.load();
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
@@ -487,3 +488,5 @@ extern "C" const char* treespec_error_string(int code) {
 extern "C" int treespec_version(void) { return 100; }
 
 extern "C" uint64_t treespec_launch_count(void) { return g_launches.load(); }
+
+extern "C" void treespec_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }

@@ -61,8 +61,8 @@ enum treespec_kernel {
     TREESPEC_KERNEL_SIMT = 1,  /* CUDA-core split-KV kernel (any dtype) */
     TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128), one 128-row query tile per CTA */
     TREESPEC_KERNEL_TC_PAIR = 3,  /* the same with two 128-row query tiles per CTA (bf16, head_dim 128, an even
-                                     number of 128-row blocks ceil(N*G / 128)); the automatic choice when its CTAs
-                                     fit the SMs in one wave and the one-tile kernel's do not */
+                                     number of 128-row blocks ceil(N*G / 128)); the automatic choice whenever the
+                                     row blocks pair up */
 };
 
 enum treespec_accept_mode {
@@ -354,6 +354,18 @@ int treespec_version(void);
 
 /* Kernels this process has launched through the library so far (all entry points). */
 uint64_t treespec_launch_count(void);
+
+/*
+ * treespec_set_wait_limit_ns -- for tests of the failure path only.  Every wait inside
+ * the tensor-core attention kernels (on a TMA copy, a tensor-core result or another warp)
+ * gives up after 2 s by default: the CTA then sets TREESPEC_STATUS_TIMEOUT, waits (with
+ * the default bound) for the copies and tensor-core work it has already started, frees
+ * its tensor memory and exits, leaving its rows incomplete.  This call sets that bound,
+ * in nanoseconds, for the tree_attn_verify calls this process makes afterwards; a bound
+ * shorter than the kernels' normal hand-offs (1 ns, say) makes them give up on purpose.
+ * 0 restores the default.  Not thread-safe against concurrent calls.
+ */
+void treespec_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }
