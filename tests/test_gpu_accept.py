@@ -39,8 +39,9 @@ def test_configs_full_size(ts, cuda_device, name, mode):
     res = run(ts, x, cuda_device, mode)
     n, ties, flipped = compare_accept(res, x.target_logits, x.draft_tokens, x.draft_probs, x.tree_parents,
                                       x.uniforms, x.temperature)
-    print(f"{name}: {n} sequences, {ties} with a rounding tie, {flipped} took the other side")
-    assert flipped <= max(1, n // 16)
+    print(f"{name}: {n} sequences, {ties} with a decision within the rounding margin, {flipped} took the "
+          f"other side")
+    assert flipped == 0
 
 
 def _small(B, N, V, parents, temperature, seed, tied=False, dup=False):
@@ -87,7 +88,8 @@ def test_edge_shapes(ts, cuda_device, T, shape, V, mode):
     N = len(parents)
     data = _small(16 if V < 40000 else 4, N, V, parents, T, seed=V + N)
     n, ties, flipped = _run_small(ts, cuda_device, *data, T, mode)
-    assert flipped <= 1
+    print(f"{shape} V={V} T={T}: {n} sequences, {ties} within the rounding margin, {flipped} took the other side")
+    assert flipped == 0
 
 
 @pytest.mark.parametrize("mode", [1, 2])

@@ -58,7 +58,7 @@ def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
 
 def test_auto_plan_picks_tensor_cores_for_bf16_head128(ts, cuda_device):
     for name, want in [("c2_llama3_8b_bf16_greedy", 2), ("c3_llama2_7b_bf16_stoch", 2),
-                       ("c4_llama3_70b_bf16_greedy", 2), ("c5_ragged_b64_bf16_stoch", 2),
+                       ("c4_llama3_70b_bf16_greedy", 3), ("c5_ragged_b64_bf16_stoch", 2),
                        ("c1_tiny_f32_greedy", 1)]:
         w = gen.get(name)
         prob = ts.AttnProblem(w.batch, w.num_nodes, w.num_q_heads, w.num_kv_heads, w.head_dim, 16, 64, 100,
@@ -148,20 +148,58 @@ def test_bad_page_id_is_flagged_not_read(ts, cuda_device):
     assert ts.read_status(ws) & 2
 
 
+def full_size_pairs(w, n, seed):
+    """n (sequence, kv head) pairs: the first and the last sequence and head, the rest drawn
+    at random.  Every pair covers all of its kv head's row blocks (all N * G rows)."""
+    rng = np.random.default_rng(seed)
+    pairs = {(0, 0), (w.batch - 1, w.num_kv_heads - 1), (0, w.num_kv_heads - 1), (w.batch - 1, 0)}
+    while len(pairs) < n:
+        pairs.add((int(rng.integers(0, w.batch)), int(rng.integers(0, w.num_kv_heads))))
+    return sorted(pairs)
+
+
 def test_full_size_bench_workload_sampled(ts, cuda_device):
-    """The bench's workload at full size; the oracle checks sampled (sequence, kv head) pairs."""
-    w = gen.get("c4_llama3_70b_bf16_greedy")
+    """The bench's workload at full size, in the bench's launch configuration (the automatic
+    plan); the oracle checks 16 (sequence, kv head) pairs, each over all four row blocks."""
+    from oracle_pool import oracle_attention_pairs
+    name = "c4_llama3_70b_bf16_greedy"
+    w = gen.get(name)
     x = gi.make_inputs(w, with_accept=False)
     d = attn_device_inputs(x, cuda_device)
-    assert ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])).kernel == ts.KERNEL_TC
+    assert ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])).kernel == ts.KERNEL_TC_PAIR
     out = run(ts, x, cuda_device)
-    rng = np.random.default_rng(0)
-    pairs = [(int(b), int(h)) for b, h in zip(rng.integers(0, w.batch, 3), rng.integers(0, w.num_kv_heads, 3))]
-    ref = oracle_attention(x, pairs)
+    pairs = full_size_pairs(w, 16, 0)
+    ref = oracle_attention_pairs(name, pairs, workers=8)
     mask = ~np.isnan(ref)
-    assert mask.sum() > 0
+    assert mask.sum() == len(pairs) * w.num_nodes * w.group * w.head_dim
     assert_attention_close(out, ref, w.dtype, mask=mask)
     assert torch.isfinite(out.float()).all()
+
+
+def test_batch8_automatic_plan_in_full(ts, cuda_device):
+    """The Llama-3-70B shape at batch 8 through the automatic plan (two-tile kernel, KV
+    split in two, merge), every (sequence, kv head) pair against the oracle."""
+    from oracle_pool import oracle_attention_pairs
+    name = "c4_llama3_70b_bf16_greedy@b8"
+    w = gen.get(name)
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    plan = ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"]))
+    assert plan.kernel == ts.KERNEL_TC_PAIR and plan.merge
+    out = run(ts, x, cuda_device)
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    ref = oracle_attention_pairs(name, pairs, workers=16)
+    assert_attention_close(out, ref, w.dtype)
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2])
+def test_llama2_mha_at_its_full_batch(ts, cuda_device, kernel):
+    """The Llama-2-7B shape (32 q / 32 kv heads, 16 nodes) at its batch of 8, in full."""
+    w = gen.get("c3_llama2_7b_bf16_stoch")
+    assert w.batch == 8
+    x = gi.make_inputs(w, with_accept=False)
+    out = run(ts, x, cuda_device, kernel=kernel)
+    assert_attention_close(out, oracle_attention(x), w.dtype)
 
 
 def test_full_size_ragged_sampled(ts, cuda_device):
@@ -183,9 +221,9 @@ def test_two_tile_kernel_refuses_an_odd_number_of_row_blocks(ts, cuda_device):
         run(ts, x, cuda_device, kernel=ts.KERNEL_TC_PAIR)
 
 
-@pytest.mark.parametrize("kernel", [2, 3])
-def test_full_size_tensor_core_kernels_agree(ts, cuda_device, kernel):
-    """Both tensor-core kernels on the full bench workload, checked on sampled pairs."""
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+def test_full_size_every_kernel_on_sampled_pairs(ts, cuda_device, kernel):
+    """Every attention kernel on the full bench workload, checked on sampled pairs."""
     w = gen.get("c4_llama3_70b_bf16_greedy")
     x = gi.make_inputs(w, with_accept=False)
     out = run(ts, x, cuda_device, kernel=kernel)
