@@ -74,6 +74,8 @@ _lib.treespec_error_string.argtypes = [ctypes.c_int]
 _lib.treespec_error_string.restype = ctypes.c_char_p
 _lib.treespec_version.restype = ctypes.c_int
 _lib.treespec_launch_count.restype = ctypes.c_uint64
+_lib.treespec_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+_lib.treespec_set_wait_limit_ns.restype = None
 
 
 class TreespecError(RuntimeError):
@@ -99,6 +101,12 @@ def version() -> int:
 
 def launch_count() -> int:
     return int(_lib.treespec_launch_count())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound (ns) of the tensor-core kernels' internal waits for later calls; 0 = the default
+    2 s.  For tests of the timeout path (see include/treespec.h)."""
+    _lib.treespec_set_wait_limit_ns(int(ns))
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

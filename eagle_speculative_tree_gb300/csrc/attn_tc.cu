@@ -55,7 +55,6 @@ constexpr uint32_t kColS = 0;
 constexpr uint32_t kColQ = 256;      // Q (bf16 pairs): [256, 320)
 constexpr uint32_t kColP = 320;      // P (bf16 pairs): [320, 384)
 constexpr uint32_t kColO = 384;      // O: [384, 512)
-constexpr uint64_t kWaitNs = 2000000000ull;
 
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr int kOffK = 0;
@@ -165,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return (jt < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
         };
         int batch_cur = fetch_batch(0), batch_next = fetch_batch(1);
+        int armed = 0;                                      // tiles whose stage this warp armed
         for (int j = 0; j < ntiles; ++j) {
             const int stage = j % nst;
             if (j > 0 && (j & 3) == 0) {
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     page = -1;
                 }
             }
-            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, kWaitNs)) {
+            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
             }
@@ -223,6 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
             }
             __syncwarp();
+            ++armed;
+        }
+        // Every copy this warp started has landed before the CTA may end: after an abort the
+        // consumers no longer wait for them.  The last phase armed on each stage completes
+        // once its copies arrive (earlier phases completed before it was armed).
+        for (int s2 = 0; s2 < nst && s2 < armed; ++s2) {
+            const int last = s2 + ((armed - 1 - s2) / nst) * nst;
+            mbar_wait_bounded(&full[s2], uint32_t(last / nst) & 1u, kDefaultWaitNs);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -235,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ry = mbar_try_wait(y, py);
             bool r = rx && ry;
             if (!__all_sync(0xffffffffu, r)) {
-                r = !*abort_flag && (rx || mbar_wait_bounded(x, px, kWaitNs)) &&
-                    (ry || mbar_wait_bounded(y, py, kWaitNs));
+                r = !*abort_flag && (rx || mbar_wait_bounded(x, px, p.wait_ns)) &&
+                    (ry || mbar_wait_bounded(y, py, p.wait_ns));
             }
             return __all_sync(0xffffffffu, r);
         };
@@ -268,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             return true;
         };
-        bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->q_full, 0, kWaitNs));
+        bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->q_full, 0, p.wait_ns));
         for (int j = 0; ok && j < kSB && j < ntiles; ++j) ok = issue_s(j);
         for (int j = 0; ok && j < ntiles; ++j) {
             // O += P_j V_j once P_j is in TMEM and V_j has landed, then S_{j+2}
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (elect_one()) mma_commit(&bars->drain);          // the pipe completes MMAs in issue order
         __syncwarp();
-        mbar_wait_bounded(&bars->drain, 0, kWaitNs);
+        mbar_wait_bounded(&bars->drain, 0, kDefaultWaitNs);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1] & mw[2] & mw[3]) == 0xffffffffu);
             const int sb = j % kSB;
             const uint32_t scol = tl + kColS + uint32_t(sb) * 128u;
-            if (!mbar_wait_bounded(&bars->s_full[sb], (j / kSB) & 1, kWaitNs)) { alive = false; break; }
+            if (!mbar_wait_bounded(&bars->s_full[sb], (j / kSB) & 1, p.wait_ns)) { alive = false; break; }
             tc_fence_after();
             if (warp_rows) {
 #pragma unroll
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l += (a0 + a1) + (a2 + a3);
             // the P buffer and O are free once P_{j-1} V_{j-1} has completed
-            if (j > 0 && !mbar_wait_bounded(&bars->pv_done, (j - 1) & 1, kWaitNs)) {
+            if (j > 0 && !mbar_wait_bounded(&bars->pv_done, (j - 1) & 1, p.wait_ns)) {
                 alive = false;
                 break;
             }
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars->p_full[sb]);
         }
-        if (!alive || !mbar_wait_bounded(&bars->pv_done, (ntiles - 1) & 1, kWaitNs)) {
+        if (!alive || !mbar_wait_bounded(&bars->pv_done, (ntiles - 1) & 1, p.wait_ns)) {
             *abort_flag = 1;
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
         } else {

@@ -53,7 +53,6 @@ constexpr int kWarpMma = 10;         // warps 10 and 11 issue the MMAs of tiles 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;        // S buffer b of tile t: [128 t + 64 b, 128 t + 64 b + 64)
 constexpr uint32_t kColO = 256;      // O_t: [256 + 128 t, 256 + 128 t + 128)
-constexpr uint64_t kWaitNs = 2000000000ull;
 // registers per thread: 168 at launch (384 threads); then the producer / issuer
 // warpgroup (warps 8-11) drops to 56 and the two softmax warpgroups rise to 200:
 // 128 x (200 + 200 + 56) = 58,368 <= 384 x 168 = 64,512
@@ -171,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return (jt < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
         };
         int batch_cur = fetch_batch(0), batch_next = fetch_batch(1);
+        int armed = 0;                                      // tiles whose stage this warp armed
         for (int j = 0; j < ntiles; ++j) {
             const int stage = j % nst;
             if (j > 0 && (j & 7) == 0) {
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     page = -1;
                 }
             }
-            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, kWaitNs)) {
+            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
             }
@@ -228,6 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
             }
             __syncwarp();
+            ++armed;
+        }
+        // Every copy this warp started has landed before the CTA may end: after an abort the
+        // consumers no longer wait for them.  The last phase armed on each stage completes
+        // once its copies arrive (earlier phases completed before it was armed).
+        for (int s2 = 0; s2 < nst && s2 < armed; ++s2) {
+            const int last = s2 + ((armed - 1 - s2) / nst) * nst;
+            mbar_wait_bounded(&full[s2], uint32_t(last / nst) & 1u, kDefaultWaitNs);
         }
       } else {
         // ------------------------------------------------------------ MMA issuers
@@ -237,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp - kWarpMma;
         auto ready = [&](uint64_t* x, uint32_t px) -> bool {
             bool r = mbar_try_wait(x, px);
-            if (!__all_sync(0xffffffffu, r)) r = !*abort_flag && (r || mbar_wait_bounded(x, px, kWaitNs));
+            if (!__all_sync(0xffffffffu, r)) r = !*abort_flag && (r || mbar_wait_bounded(x, px, p.wait_ns));
             return __all_sync(0xffffffffu, r);
         };
         constexpr uint32_t kIdS = idesc_bf16_f32(128, kBN, false);
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (elect_one()) mma_commit(&bars->drain[t]);      // the pipe completes MMAs in issue order
         __syncwarp();
-        mbar_wait_bounded(&bars->drain[t], 0, kWaitNs);
+        mbar_wait_bounded(&bars->drain[t], 0, kDefaultWaitNs);
         __syncwarp();
       }
     } else {
@@ -358,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mw[w] = row_ok ? bits : 0u;
             }
             const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
-            if (!mbar_wait_bounded(&bars->s_full[t][bf], (j >> 1) & 1, kWaitNs)) { alive = false; break; }
+            if (!mbar_wait_bounded(&bars->s_full[t][bf], (j >> 1) & 1, p.wait_ns)) { alive = false; break; }
             tc_fence_after();
             if (warp_rows) {
 #pragma unroll
@@ -404,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             if (__any_sync(0xffffffffu, resc)) {
                 // O_t may be rescaled once P_t(j-1) V(j-1) is in it (P_t(j) V(j) waits for p_full)
-                if (!mbar_wait_bounded(&bars->pv_done[t][bf ^ 1], ((j - 1) >> 1) & 1, kWaitNs)) {
+                if (!mbar_wait_bounded(&bars->pv_done[t][bf ^ 1], ((j - 1) >> 1) & 1, p.wait_ns)) {
                     alive = false;
                     break;
                 }
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars->p_full[t][bf]);
         }
-        if (!alive || !mbar_wait_bounded(&bars->o_full[t], 0, kWaitNs)) {
+        if (!alive || !mbar_wait_bounded(&bars->o_full[t], 0, p.wait_ns)) {
             *abort_flag = 1;
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
         } else {

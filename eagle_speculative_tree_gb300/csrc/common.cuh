@@ -12,6 +12,9 @@ namespace treespec {
 constexpr int kMaxNodes = 64;          // one 64-bit ancestry word per node
 constexpr int kAbsent = TREESPEC_ABSENT;   // parent entry of a padding slot past the end of a smaller tree
 constexpr size_t kWsAlign = 256;
+// Every wait inside a kernel gives up after this long (nanoseconds), sets
+// TREESPEC_STATUS_TIMEOUT and winds the CTA down.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -75,6 +78,7 @@ struct AttnParams {
     int B, N, Hq, Hkv, G, R, D, ps, max_pages, num_pool_pages;
     int num_splits, split_tokens, rows_per_block, row_blocks, merge;
     float scale_log2;             // log2(e) / sqrt(D)
+    uint64_t wait_ns;             // bound of the tensor-core kernels' pipeline waits (kDefaultWaitNs unless a test shortens it)
 };
 
 // ------------------------------------------------------------------ accept

@@ -45,6 +45,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test: true iff the phase with `parity` has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Same test, but a thread that finds the phase incomplete is suspended in hardware until
 // it completes or `hint_ns` passes, instead of spinning on issue slots that the warps
 // sharing its scheduler could use.
@@ -60,15 +73,26 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase with `parity` to complete, giving up after `limit_ns`.
-// Returns false on timeout (the caller records it and winds down).
+// Wait for the phase with `parity` to complete, giving up once `limit_ns` has passed since
+// the first failed test (checked before every sleeping retest; a retest sleeps at most
+// min(limit_ns, 20 us)).  Returns false on timeout (the caller records it and winds down).
+// try_wait itself may block in hardware for a system-dependent time, so bounds shorter
+// than 20 us (tests of the timeout path) poll with the non-blocking test_wait instead.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns < 20000u) {
+        const uint64_t t0 = global_ns();
+        do {
+            if (mbar_test_wait(bar, parity)) return true;
+        } while (global_ns() - t0 < limit_ns);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-        if (global_ns() - t0 > limit_ns) return false;
+    const uint32_t hint = limit_ns < 20000u ? uint32_t(limit_ns) : 20000u;
+    for (;;) {
+        if (global_ns() - t0 >= limit_ns) return false;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     }
-    return true;
 }
 
 // Elect one lane of the (fully active) warp: true there, false in the others.
