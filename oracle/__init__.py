@@ -5,7 +5,7 @@ from the method's description; the CUDA library is checked against it.  Only
 the test suite, the package smoke check and the bench's CPU-baseline leg may
 import it.  It shares no code with the CUDA path and never imports it.
 
-  tree_mask   -- ancestor sets, the dense tree mask M and the 64-bit masks
+  tree_mask   -- ancestor sets, the dense tree mask M and its 64-bit words
   attention   -- tree attention over a paged KV cache (a definition)
   accept      -- greedy and rejection-sampling accept walks (an algorithm)
   kv_commit   -- keeping the accepted path's K/V after the walk (a definition)

@@ -9,6 +9,12 @@ word with (1 << j).
 The tree arrives as a parent array in topological order: parents[0] = -1
 (the root, i.e. the last verified token) and 0 <= parents[i] < i.
 
+Trees larger than 64 nodes ("EAGLE-2 & Lookahead Decoding", section 6: the tree size
+follows the load, so a lightly loaded server verifies bigger trees; the radar page's
+single word stops at 64).  Reading: the same relation for up to 128 nodes is two 64-bit
+words per node, word w holding bits 64w .. 64w+63 of the set; "is j an ancestor of i"
+tests bit j % 64 of word j // 64.
+
 A batch may hold trees of different sizes ("EAGLE-2 & Lookahead Decoding",
 section 6, "Batched Dynamic Tree Slicing": the tree is cut to fewer tokens under
 load).  Reading: each row of the batch's parent array is padded to the batch's
@@ -74,6 +80,16 @@ def ancestor_bitmasks(parents) -> list[int]:
     if n > 64:
         raise ValueError("a 64-bit ancestry mask holds at most 64 nodes")
     return [sum(1 << j for j in range(n) if m[i, j]) for i in range(n)]
+
+
+def ancestor_words(parents, n_words: int = 2) -> list[list[int]]:
+    """words[i][w] = bits 64w .. 64w+63 of mask_i (bit j set iff M[i][j]); N <= 64 * n_words."""
+    m = mask_matrix(parents)
+    n = len(parents)
+    if n > 64 * n_words:
+        raise ValueError(f"{n_words} 64-bit words hold at most {64 * n_words} nodes")
+    return [[sum(1 << (j - 64 * w) for j in range(64 * w, min(n, 64 * w + 64)) if m[i, j])
+             for w in range(n_words)] for i in range(n)]
 
 
 def children(parents, i: int) -> list[int]:

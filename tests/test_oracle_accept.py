@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 from scipy import special, stats
 
+from gen import trees
 from gen import mc
 from oracle import accept as oacc
 
@@ -61,6 +62,51 @@ def test_greedy_equals_brute_force_on_all_small_trees(n):
             w = oacc.greedy_walk(logits, tokens, parents)
             ref_path, ref_bonus = brute_force_greedy(logits, tokens, parents)
             assert w.path == ref_path and w.bonus == ref_bonus
+
+
+def longest_matching_path_by_dfs(logits, tokens, parents):
+    """Independent statement for large trees: depth-first search from the root over the
+    children whose token is the argmax of their parent's row; the deepest node reached
+    (ties: the one whose root path comes first in node order) ends the path."""
+    n = len(parents)
+    kids = {i: [c for c in range(1, n) if parents[c] == i] for i in range(n)}
+    best = []
+
+    def dfs(node, path):
+        nonlocal best
+        if len(path) > len(best):
+            best = list(path)
+        a = int(np.argmax(logits[node]))
+        for c in kids[node]:
+            if tokens[c] == a:
+                dfs(c, path + [c])
+
+    dfs(0, [])
+    last = best[-1] if best else 0
+    return best, int(np.argmax(logits[last]))
+
+
+@pytest.mark.parametrize("n", [65, 100, 128])
+def test_greedy_on_trees_past_64_nodes_equals_dfs(n):
+    """Distinct sibling tokens make the matching path unique; the walk must find it."""
+    rng = np.random.default_rng(n)
+    V = 512
+    for trial in range(20):
+        parents = trees.chain(n) if trial == 0 else trees.random_recursive(rng, n)
+        logits = rng.normal(0, 3, (n, V)).astype(np.float32)
+        tokens = np.zeros(n, dtype=np.int32)
+        for p in range(n):
+            kids = [c for c in range(1, n) if parents[c] == p]
+            if not kids:
+                continue
+            toks = rng.permutation(V)[: len(kids)]           # distinct siblings
+            a = int(np.argmax(logits[p]))
+            if rng.random() < 0.8 and a not in toks:         # the argmax sits on one child most of the time
+                toks[rng.integers(0, len(kids))] = a
+            tokens[kids] = toks
+        w = oacc.greedy_walk(logits, tokens, parents)
+        ref_path, ref_bonus = longest_matching_path_by_dfs(logits, tokens, parents)
+        assert w.path == ref_path and w.bonus == ref_bonus
 
 
 def _golden(name):

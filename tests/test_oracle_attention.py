@@ -114,6 +114,36 @@ def test_invalid_parents_rejected(bad):
 def test_bitmask_limit():
     with pytest.raises(ValueError):
         tree_mask.ancestor_bitmasks(trees.chain(65))
+    with pytest.raises(ValueError):
+        tree_mask.ancestor_words(trees.chain(129), 2)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("n", [65, 100, 128])
+def test_two_word_masks_are_the_dense_mask(seed, n):
+    """Trees past 64 nodes: bit j % 64 of word j // 64 equals the matrix-power closure."""
+    rng = np.random.default_rng(200 + seed)
+    p = trees.random_recursive(rng, n)
+    m = closure_by_matrix_powers(p)
+    words = tree_mask.ancestor_words(p, 2)
+    for i in range(n):
+        for j in range(n):
+            assert bool((words[i][j // 64] >> (j % 64)) & 1) == m[i, j]
+        assert words[i][1] == 0 or n > 64
+
+
+def test_two_word_masks_closed_forms():
+    """A chain of 128: node i holds bits 0..i.  A star of 128: the root and itself.
+    A tree of at most 64 nodes: word 0 is the single-word mask, word 1 is empty."""
+    for i, (w0, w1) in enumerate(tree_mask.ancestor_words(trees.chain(128), 2)):
+        full = (1 << (i + 1)) - 1
+        assert (w0, w1) == (full & (2**64 - 1), full >> 64)
+    for i, (w0, w1) in enumerate(tree_mask.ancestor_words(trees.star(128), 2)):
+        bits = {0, i}
+        assert w0 == sum(1 << j for j in bits if j < 64) and w1 == sum(1 << (j - 64) for j in bits if j >= 64)
+    p = trees.random_recursive(np.random.default_rng(5), 64)
+    assert [w[0] for w in tree_mask.ancestor_words(p, 2)] == tree_mask.ancestor_bitmasks(p)
+    assert all(w[1] == 0 for w in tree_mask.ancestor_words(p, 2))
 
 
 # ---------------------------------------------------------------- attention
@@ -137,11 +167,12 @@ def test_chain_equals_causal_attention(S):
     np.testing.assert_allclose(out[0], ref[:, S:, :].transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(8))
 def test_node_equals_attention_along_its_root_path(seed):
-    """Every node's output is plain attention over prefix + its root->node path, laid out contiguously."""
+    """Every node's output is plain attention over prefix + its root->node path, laid out
+    contiguously; seeds 6 and 7 draw trees past 64 nodes (up to 128)."""
     rng = np.random.default_rng(1000 + seed)
-    B, N, Hq, Hkv, D = 2, int(rng.integers(2, 20)), 8, 2, 32
+    B, N, Hq, Hkv, D = 2, int(rng.integers(2, 20) if seed < 6 else rng.integers(65, 129)), 8, 2, 32
     prefix = rng.integers(0, 70, B)
     c = make_case(rng, B, N, Hq, Hkv, D, prefix)
     out = run_oracle(c)
