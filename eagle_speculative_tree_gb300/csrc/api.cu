@@ -146,7 +146,7 @@ AttnLayout attn_layout(const treespec_attn_shape& s, const AttnPlan& p) {
     L.status = off;
     off += kWsAlign;
     L.anc = off;
-    off = align_up(off + size_t(s.batch) * s.num_nodes * 8, kWsAlign);
+    off = align_up(off + size_t(s.batch) * s.num_nodes * kAncWords * 8, kWsAlign);
     L.lens = off;
     off = align_up(off + size_t(s.batch) * 4, kWsAlign);
     L.nn = off;

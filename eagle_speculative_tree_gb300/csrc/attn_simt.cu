@@ -6,7 +6,7 @@
 // range of logical tokens (a "split"), the flash-style partial state
 //     m_r = max_t s_rt,  l_r = sum_t 2^(s_rt - m_r),  acc_r = sum_t 2^(s_rt - m_r) V_t
 // with s_rt = log2(e)/sqrt(D) * q_r . K_t over the tokens row r may see: every
-// prefix token, and tree token S + j only if bit j of node i's ancestor word is set
+// prefix token, and tree token S + j only if node i's ancestor-or-self set holds j
 // ("Tech Radar: SGLang EAGLE-2", section 2 mask M; section 5 item 1 bitmask test).
 // The kernel streams each K/V page of its split once through shared memory for all
 // of its rows (the siblings' shared prefix is read once, section 5 item 3), in
@@ -110,7 +110,7 @@ __host__ __device__ inline SimtShape simt_shape(int rows_block) {
     size_t scratch = size_t(s.nwarps) * 8 * (D + 2) * 4;
     s.kv_bytes = 2 * s.stage_bytes > scratch ? 2 * s.stage_bytes : scratch;
     s.pt_bytes = size_t(s.nwarps) * 32 * 8 * 4;
-    s.smem = s.qs_bytes + s.kv_bytes + s.pt_bytes + kMaxNodes * 8;
+    s.smem = s.qs_bytes + s.kv_bytes + s.pt_bytes + kMaxNodes * kAncWords * 8;
     return s;
 }
 
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnParams p) {
         }
         Qs[e] = v;
     }
-    for (int e = tid; e < p.N; e += nthr) anc_s[e] = p.anc[size_t(b) * p.N + e];
+    for (int e = tid; e < p.N * kAncWords; e += nthr) anc_s[e] = p.anc[size_t(b) * p.N * kAncWords + e];
 
     const int* ptab = p.page_table + size_t(b) * p.max_pages;
     auto issue = [&](int tile, int stage) {
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(AttnParams p) {
             for (int r = 0; r < 8; ++r) {
                 const int lr = rw * 8 + r;
                 bool ok = tok_ok && lr < rows;
-                if (ok && j >= 0) ok = (anc_s[(r0 + lr) / p.G] >> j) & 1ull;
+                if (ok && j >= 0) ok = (anc_s[(r0 + lr) / p.G * kAncWords + (j >> 6)] >> (j & 63)) & 1ull;
                 const float sv = ok ? s[r] : -INFINITY;
                 const float mnew = fmaxf(m[r], warp_max(sv));
                 const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(m[r] - mnew);

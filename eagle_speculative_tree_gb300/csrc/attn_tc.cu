@@ -22,7 +22,7 @@
 //     tile's columns, so a row's maximum needs no exchange between warps) stage Q into
 //     TMEM, then per tile read S from TMEM,
 //     apply the tree mask -- prefix tokens always, tree token S+j only when bit j of
-//     the node's ancestor word is set ("Tech Radar: SGLang EAGLE-2", section 2 mask M
+//     the node's ancestor set holds ("Tech Radar: SGLang EAGLE-2", section 2 mask M
 //     and section 5 bitmask) -- run the online softmax in base 2, write P as packed
 //     bf16 into the P buffer once P_{j-1} V_{j-1} has read it, and rescale O in TMEM
 //     (after that MMA too) only when a row's running max grows by more than 2^8.
@@ -63,7 +63,7 @@ constexpr int kOffBar = kOffV + kNSV * kTile;
 constexpr int kNumBars = 2 * kNSK + 2 * kNSV + 2 * kSB + 3;   // k/v full/empty, s_full, p_full, pv_done, q_full, drain
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffAnc = kOffMisc + 16;
-constexpr int kSmemBytes = kOffAnc + kMaxNodes * 8;          // 230,072 bytes: within the 227 KB limit
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * kAncWords * 8;          // 231,608 bytes: within the 227 KB limit
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int e = tid; e < p.N; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N + e];
+    for (int e = tid; e < p.N * kAncWords; e += kThreads) anc_s[e] = p.anc[size_t(b) * p.N * kAncWords + e];
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -315,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = row_in ? r / p.G : 0;
         const int hq = h * p.G + (row_in ? r % p.G : 0);
         const bool row_ok = row_in && i < nb;                // a padding slot's row is not computed
-        const uint64_t anc = row_ok ? anc_s[i] : 0ull;
+        const uint64_t anc0 = row_ok ? anc_s[i * kAncWords] : 0ull;     // the node's ancestor-or-self set
+        const uint64_t anc1 = row_ok ? anc_s[i * kAncWords + 1] : 0ull;
         const bool warp_rows = __any_sync(0xffffffffu, row_ok);
         const uint32_t tl = tbase + (uint32_t(quarter * 32) << 16);
         {
@@ -358,10 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t bits = np == 32 ? 0xffffffffu : ((1u << np) - 1u);
                 const int nh = min(max(tree_hi - lo, 0), 32);
                 const uint32_t hi_mask = nh == 32 ? 0xffffffffu : ((1u << nh) - 1u);
-                uint32_t tb = 0;
-                const int sh = lo - tree_lo;               // anc bit index of column lo
-                if (sh >= 0) tb = sh < 64 ? uint32_t(anc >> sh) : 0u;
-                else tb = -sh < 32 ? uint32_t(anc << (-sh)) : 0u;
+                const uint32_t tb = anc_bits32(anc0, anc1, lo - tree_lo);   // set bit of column lo: lo - tree_lo
                 bits |= tb & hi_mask;
                 mw[w] = row_ok ? bits : 0u;
             }

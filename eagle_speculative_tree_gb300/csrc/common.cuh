@@ -9,7 +9,11 @@
 
 namespace treespec {
 
-constexpr int kMaxNodes = 64;          // one 64-bit ancestry word per node
+// Tree nodes per sequence.  A node's ancestor-or-self set is kAncWords 64-bit words
+// (word w holds nodes 64w .. 64w+63): one word covers the 64-node trees of the radar
+// page's single-word mask, two cover trees of up to 128 nodes.
+constexpr int kMaxNodes = 128;
+constexpr int kAncWords = 2;
 constexpr int kAbsent = TREESPEC_ABSENT;   // parent entry of a padding slot past the end of a smaller tree
 constexpr size_t kWsAlign = 256;
 // Every wait inside a kernel gives up after this long (nanoseconds), sets
@@ -27,6 +31,17 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
     if ((u & 0x7fffffffu) > 0x7f800000u) return uint16_t((u >> 16) | 0x40u);   // NaN stays NaN
     u += 0x7fffu + ((u >> 16) & 1u);
     return uint16_t(u >> 16);
+}
+
+// Bits sh .. sh+31 of a 128-bit ancestor set {a0, a1} (bit j of the set = node j), as one
+// 32-bit word; positions outside 0..127 read as 0.  sh may be negative (down to -31).
+__device__ __forceinline__ uint32_t anc_bits32(uint64_t a0, uint64_t a1, int sh) {
+    if (sh <= -32 || sh >= 128) return 0u;
+    if (sh < 0) return uint32_t(a0 << (-sh));
+    if (sh >= 64) return uint32_t(a1 >> (sh - 64));
+    uint64_t w = a0 >> sh;
+    if (sh > 32) w |= a1 << (64 - sh);
+    return uint32_t(w);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -70,7 +85,7 @@ struct AttnParams {
     const int32_t* parents;       // caller's array (read by the prologue only)
     void* out;
     uint32_t* status;
-    uint64_t* anc;                // [B][N] ancestor-or-self words
+    uint64_t* anc;                // [B][N][kAncWords] ancestor-or-self sets
     int32_t* lens;                // [B] validated prefix lengths, -1 = invalid sequence
     int32_t* nn;                  // [B] nodes of each tree: parent entries before the first kAbsent
     float* part_ml;               // [B][Hkv][splits][R][2]  (m in log2 units, l)

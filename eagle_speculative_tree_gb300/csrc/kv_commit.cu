@@ -14,9 +14,11 @@ namespace {
 
 constexpr int kCommitThreads = 256;
 constexpr int kMaxRowWords = 128 * 4 / 16;              // a float32 row of head dim 128
+// staging for up to N - 1 accepted rows of one kv head (dynamic shared memory)
+constexpr int kMaxStageBytes = (kMaxNodes - 1) * kMaxRowWords * 16;
 
 __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(const CommitParams p) {
-    __shared__ uint4 buf[(kMaxNodes - 1) * kMaxRowWords];   // up to 63 rows of one kv head
+    extern __shared__ uint4 buf[];                        // [N - 1][words]: the accepted rows of one kv head
     __shared__ int s_ok, s_len, s_S, s_badpage;
     const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int* path = p.path + size_t(b) * p.N;
@@ -73,12 +75,12 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(const CommitP
         void* base = t == 0 ? p.k : p.v;
         for (int e = tid; e < n * words; e += kCommitThreads) {
             const int k = e / words, w = e % words;
-            buf[k * kMaxRowWords + w] = *row_word(base, S + path[k], w);
+            buf[k * words + w] = *row_word(base, S + path[k], w);
         }
         __syncthreads();
         for (int e = tid; e < n * words; e += kCommitThreads) {
             const int k = e / words, w = e % words;
-            *row_word(base, S + 1 + k, w) = buf[k * kMaxRowWords + w];
+            *row_word(base, S + 1 + k, w) = buf[k * words + w];
         }
         __syncthreads();
     }
@@ -88,7 +90,11 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(const CommitP
 }  // namespace
 
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s) {
-    kv_commit_kernel<<<dim3(unsigned(p.B), unsigned(p.Hkv)), kCommitThreads, 0, s>>>(p);
+    const int smem = max(16, (p.N - 1) * (p.D * p.elem / 16) * 16);
+    if (smem > kMaxStageBytes) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kv_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxStageBytes);
+    if (e != cudaSuccess) return e;
+    kv_commit_kernel<<<dim3(unsigned(p.B), unsigned(p.Hkv)), kCommitThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -1,9 +1,11 @@
-// Tree prologue: parent array -> 64-bit ancestor-or-self words, plus validation.
+// Tree prologue: parent array -> ancestor-or-self sets, plus validation.
 //
 // "Tech Radar: SGLang EAGLE-2", section 2: node i may attend to node j iff j is an
 // ancestor of i or j == i; section 5 item 1: with at most 64 nodes the relation is
-// one 64-bit word per node and the test is (word_i >> j) & 1.  The word of node i is
-// its own bit OR the bits of every node on its parent chain.
+// one 64-bit word per node and the test is (word_i >> j) & 1.  Trees of up to 128 nodes
+// ("EAGLE-2 & Lookahead Decoding", section 6: the tree grows when the load is light) use
+// two words per node, word w holding nodes 64w .. 64w+63.  The set of node i is its own
+// bit OR the bits of every node on its parent chain.
 //
 // A batch may hold trees of different sizes ("EAGLE-2 & Lookahead Decoding", section 6,
 // batched dynamic tree slicing): a row of the parent array is padded with kAbsent after
@@ -13,7 +15,7 @@
 
 namespace treespec {
 
-__global__ void __launch_bounds__(64) tree_prologue_kernel(AttnParams p) {
+__global__ void __launch_bounds__(kMaxNodes) tree_prologue_kernel(AttnParams p) {
     __shared__ int par[kMaxNodes];
     __shared__ int bad, first_pad;
     const int b = blockIdx.x, i = threadIdx.x, N = p.N;
@@ -40,12 +42,16 @@ __global__ void __launch_bounds__(64) tree_prologue_kernel(AttnParams p) {
     }
     __syncthreads();
     if (i < N) {
-        uint64_t w = 0;
+        static_assert(kAncWords == 2, "two words per node");
+        uint64_t w0 = 0, w1 = 0;                                  // nodes 0..63, 64..127
         if (i < nb) {
-            w = 1ull << i;
-            for (int j = par[i]; j >= 0; j = par[j]) w |= 1ull << j;   // par[j] < j: at most i steps
+            for (int j = i; j >= 0; j = par[j]) {                 // i, then its parent chain (par[j] < j)
+                if (j < 64) w0 |= 1ull << j;
+                else w1 |= 1ull << (j - 64);
+            }
         }
-        p.anc[(size_t)b * N + i] = w;
+        p.anc[((size_t)b * N + i) * kAncWords] = w0;
+        p.anc[((size_t)b * N + i) * kAncWords + 1] = w1;
     }
     if (i == 0) {
         p.nn[b] = nb;
@@ -59,7 +65,7 @@ __global__ void __launch_bounds__(64) tree_prologue_kernel(AttnParams p) {
 }
 
 cudaError_t launch_tree_prologue(const AttnParams& p, cudaStream_t s) {
-    tree_prologue_kernel<<<p.B, 64, 0, s>>>(p);
+    tree_prologue_kernel<<<p.B, kMaxNodes, 0, s>>>(p);
     return cudaGetLastError();
 }
 

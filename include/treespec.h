@@ -6,7 +6,9 @@
  *   - "Tech Radar: SGLang EAGLE-2", section 2 (Dynamic Tree-Attention Verification):
  *     each draft node attends only to its tree ancestors and itself, on top of the
  *     cached prefix; section 5 item 1: for trees of at most 64 nodes the ancestor
- *     relation is one 64-bit word per node, tested with a single AND.
+ *     relation is one 64-bit word per node, tested with a single AND.  Trees of up
+ *     to 128 nodes ("EAGLE-2 & Lookahead Decoding", section 6: the tree size follows
+ *     the load) use two such words per node.
  *   - "Speculative Decoding in Production: EAGLE-3 Dynamic Trees", section
  *     "Mathematical Proof of Lossless Speedup", steps 1-3: accept a draft token with
  *     probability min(1, p/q), otherwise resample from the normalised max(0, p - q);
@@ -30,7 +32,7 @@
  *     offending element is skipped (never dereferenced), and the caller reads the word
  *     with treespec_read_status() after the call.
  *   - Tree layout: tree_parents[b][0] = -1 is the root (the last verified token) and
- *     0 <= tree_parents[b][i] < i for i >= 1 (topological order), N <= 64.
+ *     0 <= tree_parents[b][i] < i for i >= 1 (topological order), N <= 128.
  *     Trees of different sizes share a batch ("EAGLE-2 & Lookahead Decoding", section
  *     6, batched dynamic tree slicing): sequence b's tree is the N_b <= N entries
  *     before the first TREESPEC_ABSENT (-2) of its row, and every later entry must be
@@ -97,7 +99,7 @@ enum treespec_status_bits {
 
 typedef struct {
     int32_t batch;              /* B >= 1 */
-    int32_t num_nodes;          /* N, tree nodes including the root, 1..64 */
+    int32_t num_nodes;          /* N, tree nodes including the root, 1..128 */
     int32_t num_q_heads;        /* Hq */
     int32_t num_kv_heads;       /* Hkv, Hq % Hkv == 0; G = Hq / Hkv query heads share a kv head */
     int32_t head_dim;           /* D: 64 or 128 */
@@ -222,7 +224,7 @@ size_t treespec_accept_workspace_bytes(int32_t batch, int32_t num_nodes, int32_t
  *                                    padded with -1
  *   accept_len    [B]       int32    out: number of accepted draft nodes
  *   bonus_token   [B]       int32    out
- * Limits: N in 1..64, V in 1..2^30.  A draft token outside [0, V) is rejected and
+ * Limits: N in 1..128, V in 1..2^30.  A draft token outside [0, V) is rejected and
  * flagged with TREESPEC_STATUS_BAD_TOKEN.
  * target_logits and draft_probs may point to device memory or to host memory the device
  * can address (pinned, e.g. from cudaHostAlloc): the kernels then read the rows in place
@@ -333,7 +335,7 @@ int tree_draft_step(const float *logprobs, int32_t batch, int32_t frontier, int3
  * draft_tokens [B][num_nodes].  A parent index that is not smaller than its node's, or
  * a kept node whose parent was dropped (possible only with positive log-probabilities),
  * is attached to the root and sets TREESPEC_STATUS_BAD_PARENT.
- * Limits: 1 <= num_nodes <= min(64, max_nodes), max_nodes <= 1024.
+ * Limits: 1 <= num_nodes <= min(128, max_nodes), max_nodes <= 1024.
  */
 int tree_rerank(const int32_t *node_parent, const int32_t *node_token, const float *node_score,
                 int32_t batch, int32_t max_nodes, int32_t num_nodes,

@@ -43,7 +43,7 @@ def shape(**kw):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(num_nodes=65), dict(num_nodes=0), dict(num_q_heads=30), dict(head_dim=96),
+    dict(num_nodes=129), dict(num_nodes=0), dict(num_q_heads=30), dict(head_dim=96),
     dict(page_size=32), dict(batch=0), dict(dtype=7), dict(max_pages_per_seq=0),
     dict(num_splits=-1), dict(kernel=9),
     dict(kernel=3),                       # two-tile kernel: 8 nodes x 4 query heads is one 128-row block
@@ -99,7 +99,7 @@ def test_accept_rejects_bad_arguments():
         return lib.tree_accept(logits, FAKE, probs, FAKE, unif, ctypes.c_float(temp), FAKE, FAKE, FAKE,
                                B, N, V, ws, wsb, None)
 
-    assert call(N=65) == -2
+    assert call(N=129) == -2
     assert call(B=0) == -2
     assert call(V=0) == -2
     assert call(logits=None) == -1
@@ -110,7 +110,7 @@ def test_accept_rejects_bad_arguments():
     assert call(logits=FAKE + 8) == -6
     assert call(ws=FAKE + 64) == -4
     assert call(wsb=16) == -4
-    assert lib.treespec_accept_workspace_bytes(2, 65, 100) == 0
+    assert lib.treespec_accept_workspace_bytes(2, 129, 100) == 0
 
 
 def test_valid_call_without_device_reports_no_device():

@@ -79,12 +79,14 @@ def _run_small(ts, device, logits, tokens, q, parents, u, T, mode=0):
 
 @pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("T", [0.0, 1.0, 0.05, 20.0])
-@pytest.mark.parametrize("shape", ["root_only", "chain64", "star64", "random64", "mtp"])
+@pytest.mark.parametrize("shape", ["root_only", "chain64", "star64", "random64", "mtp", "chain128", "star128",
+                                   "random128"])
 @pytest.mark.parametrize("V", [7, 256, 5003, 40000])
 def test_edge_shapes(ts, cuda_device, T, shape, V, mode):
     rng = np.random.default_rng(V)
     parents = {"root_only": [-1], "chain64": trees.chain(64), "star64": trees.star(64),
-               "random64": trees.random_recursive(rng, 64), "mtp": [-1, 0]}[shape]
+               "random64": trees.random_recursive(rng, 64), "mtp": [-1, 0], "chain128": trees.chain(128),
+               "star128": trees.star(128), "random128": trees.random_recursive(rng, 128)}[shape]
     N = len(parents)
     data = _small(16 if V < 40000 else 4, N, V, parents, T, seed=V + N)
     n, ties, flipped = _run_small(ts, cuda_device, *data, T, mode)

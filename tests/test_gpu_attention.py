@@ -89,7 +89,7 @@ def _custom(name, parents, prefix, batch=None):
                                               ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2),
                                               ("c4_llama3_70b_bf16_greedy", 3)])
 @pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
-                                  "random64", "random32"])
+                                  "random64", "random32", "chain128", "star128", "random128", "random100"])
 def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
     rng = np.random.default_rng(hash(case) % 2**32)
     if case == "single_node":
@@ -104,6 +104,14 @@ def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
         parents, prefix = [trees.star(64)], [40]
     elif case == "random32":
         parents, prefix = [trees.random_recursive(rng, 32), trees.random_recursive(rng, 32)], [700, 3]
+    elif case == "chain128":                       # trees past 64 nodes: two ancestor words per node
+        parents, prefix = [trees.chain(128)], [300]
+    elif case == "star128":
+        parents, prefix = [trees.star(128)], [77]
+    elif case == "random128":
+        parents, prefix = [trees.random_recursive(rng, 128), trees.random_recursive(rng, 128)], [0, 517]
+    elif case == "random100":
+        parents, prefix = [trees.random_recursive(rng, 100)], [129]
     else:
         parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
     w, x = _custom(dtype_cfg, parents, prefix)

@@ -68,19 +68,19 @@ def test_commit_matches_oracle(ts, cuda_device, name, batch, seed):
     assert st == 0 and want == 0
 
 
-@pytest.mark.parametrize("shape", ["chain64", "star64", "random64"])
+@pytest.mark.parametrize("shape", ["chain64", "star64", "random64", "chain128", "random128"])
 def test_commit_edge_trees(ts, cuda_device, shape):
     from dataclasses import replace
-    n = 64
-    make = {"chain64": lambda r: trees.chain(n), "star64": lambda r: trees.star(n),
-            "random64": lambda r: trees.random_recursive(r, n)}[shape]
+    n = int(shape[-3:]) if shape.endswith("128") else 64
+    make = {"chain": lambda r: trees.chain(n), "star": lambda r: trees.star(n),
+            "random": lambda r: trees.random_recursive(r, n)}[shape.rstrip("0123456789")]
     rng = np.random.default_rng(5)
     parents = np.stack([make(rng) for _ in range(3)]).astype(np.int32)
     w = replace(gen.get("c2_llama3_8b_bf16_greedy").with_batch(3), num_nodes=n)
     x = gi.make_inputs(w, parents=parents, prefix_lens=np.array([0, 15, 200], dtype=np.int32), with_accept=False)
     path, lens = random_paths(x.tree_parents, 3, stop_prob=0.0)     # walk to a leaf
-    if shape == "chain64":
-        assert lens.tolist() == [63] * 3                            # the whole chain: nothing moves
+    if shape.startswith("chain"):
+        assert lens.tolist() == [n - 1] * 3                         # the whole chain: nothing moves
     st, want = run_both(ts, x, cuda_device, path, lens)
     assert st == 0 and want == 0
 

@@ -56,6 +56,7 @@ def build_both(ts, device, B, V, k, steps, N, seed, ties=False):
     (2, 128256, 8, 6, 64),      # Llama-3 vocabulary, the 64-node tree
     (3, 1001, 16, 2, 24),       # scalar loads (V % 4 != 0), the largest branching
     (2, 5003, 1, 7, 8),         # topk 1: the greedy chain
+    (2, 32000, 8, 6, 128),      # a 128-node tree: two ancestor words per node downstream
 ])
 @pytest.mark.parametrize("ties", [False, True])
 def test_draft_tree_matches_oracle(ts, cuda_device, B, V, k, steps, N, ties):

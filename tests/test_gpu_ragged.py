@@ -50,6 +50,24 @@ def test_attention_over_trees_of_different_sizes(ts, cuda_device, kernel, splits
         assert torch.all(out[b, n:] == 0)
 
 
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+def test_attention_over_trees_of_up_to_128_nodes_of_different_sizes(ts, cuda_device, kernel):
+    """A batch of 128-node rows holding trees of 128, 65, 64 and 3 nodes."""
+    from dataclasses import replace
+    rng = np.random.default_rng(17)
+    sizes, prefix = [128, 65, 64, 3], [90, 1000, 0, 33]
+    w = replace(gen.get("c4_llama3_70b_bf16_greedy").with_batch(len(sizes)), num_nodes=128)
+    parents = trees.padded([trees.random_recursive(rng, n) for n in sizes], w.num_nodes)
+    x = gi.make_inputs(w, parents=parents, prefix_lens=np.asarray(prefix, dtype=np.int32), with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    out = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"],
+                              d["tree_parents"], kernel=kernel)
+    torch.cuda.synchronize()
+    assert_attention_close(out, oracle_attention(x), w.dtype)
+    for b, n in enumerate(sizes):
+        assert torch.all(out[b, n:] == 0)
+
+
 def test_attention_flags_a_node_after_the_padding(ts, cuda_device):
     w = gen.get("c2_llama3_8b_bf16_greedy").with_batch(1)
     x = gi.make_inputs(w, parents=np.asarray([[-1, 0, trees.PAD, 1, trees.PAD, trees.PAD, trees.PAD, trees.PAD]],

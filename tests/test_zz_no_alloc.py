@@ -81,7 +81,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(ts, cuda_device):
     out = torch.zeros_like(d["q"])
     assert _noalloc(ts, d, out, prob) == -4
     bad = ts.attn_problem(d["q"], d["k_pages"], d["page_table"])
-    bad.num_nodes = 65
+    bad.num_nodes = 129
     assert _noalloc(ts, d, out, bad) == -2
 
 
