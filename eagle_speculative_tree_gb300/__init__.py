@@ -25,7 +25,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC_PAIR = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC_PAIR, KERNEL_TC_2SM = 0, 1, 2, 3, 4
 ACCEPT_AUTO, ACCEPT_ALL_ROWS, ACCEPT_PATH_ONLY = 0, 1, 2
 ABSENT = -2                     # parent entry of a padding slot after a smaller tree
 STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT", 32: "INTERNAL",
@@ -76,6 +76,8 @@ _lib.treespec_version.restype = ctypes.c_int
 _lib.treespec_launch_count.restype = ctypes.c_uint64
 _lib.treespec_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
 _lib.treespec_set_wait_limit_ns.restype = None
+_lib.treespec_last_launch_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+_lib.treespec_last_launch_error.restype = ctypes.c_int
 
 
 class TreespecError(RuntimeError):
@@ -92,7 +94,9 @@ def _check(code: int) -> None:
 def exported_symbols() -> list[str]:
     """Function names declared in include/treespec.h."""
     text = open(HEADER_PATH).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, re.M)))
+    # declarations start in column 0 with a C return type; comment lines never do
+    return sorted(set(re.findall(r"^(?:const\s+)?(?:int|size_t|void|uint64_t|uint32_t|char)\s*\*?\s*([a-z_0-9]+)\s*\(",
+                                 text, re.M)))
 
 
 def version() -> int:
@@ -101,6 +105,13 @@ def version() -> int:
 
 def launch_count() -> int:
     return int(_lib.treespec_launch_count())
+
+
+def last_launch_error() -> tuple:
+    """(cudaError_t code, its name) behind the last launch the CUDA runtime rejected."""
+    name = ctypes.c_char_p()
+    code = _lib.treespec_last_launch_error(ctypes.byref(name))
+    return code, (name.value or b"").decode()
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -12,6 +12,13 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};     // see treespec_set_wait_limit_ns
+std::atomic<int> g_launch_error{0};                 // cudaError_t of the last rejected launch
+
+// TREESPEC_ERR_LAUNCH for a launch the runtime rejected, keeping the runtime's code
+int launch_failed(cudaError_t e) {
+    g_launch_error.store(int(e));
+    return TREESPEC_ERR_LAUNCH;
+}
 
 constexpr int kDefaultSms = 152;
 constexpr int kMaxDevices = 64;
@@ -64,13 +71,14 @@ int check_attn_shape(const treespec_attn_shape* s) {
     if ((long long)s->max_pages_per_seq * s->page_size > (1ll << 30)) return TREESPEC_ERR_SHAPE;
     const long long R = (long long)s->num_nodes * (s->num_q_heads / s->num_kv_heads);
     if (R > 4096 || (long long)s->num_kv_heads * ((R + 63) / 64) > 65535) return TREESPEC_ERR_SHAPE;
-    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC_PAIR) return TREESPEC_ERR_SHAPE;
+    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC_2SM) return TREESPEC_ERR_SHAPE;
     if (s->num_splits < 0) return TREESPEC_ERR_SHAPE;
-    if (s->kernel == TREESPEC_KERNEL_TC || s->kernel == TREESPEC_KERNEL_TC_PAIR) {
+    if (s->kernel == TREESPEC_KERNEL_TC || s->kernel == TREESPEC_KERNEL_TC_PAIR || s->kernel == TREESPEC_KERNEL_TC_2SM) {
         if (!attn_tc_supported(s->dtype, s->head_dim)) return TREESPEC_ERR_DTYPE;
         if ((long long)s->num_pool_pages * s->page_size >= (1ll << 31)) return TREESPEC_ERR_SHAPE;
     }
-    if (s->kernel == TREESPEC_KERNEL_TC_PAIR && ((R + 127) / 128) % 2 != 0) return TREESPEC_ERR_SHAPE;
+    if ((s->kernel == TREESPEC_KERNEL_TC_PAIR || s->kernel == TREESPEC_KERNEL_TC_2SM) && ((R + 127) / 128) % 2 != 0)
+        return TREESPEC_ERR_SHAPE;
     return TREESPEC_OK;
 }
 
@@ -86,10 +94,11 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     // each K/V tile for 256 query rows, the one-tile kernel for 128, and the L2 reads of the
     // one-tile kernel bind first (32 x 8192 tokens, 64 q / 8 kv heads, 64 nodes: 0.471 ms
     // against 0.541 at batch 32, 0.244 against 0.317 at batch 16).
-    if (s.kernel == TREESPEC_KERNEL_TC || s.kernel == TREESPEC_KERNEL_TC_PAIR ||
+    if (s.kernel == TREESPEC_KERNEL_TC || s.kernel == TREESPEC_KERNEL_TC_PAIR || s.kernel == TREESPEC_KERNEL_TC_2SM ||
         (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
         const bool paired = ((R + 127) / 128) % 2 == 0;
-        p.kernel = s.kernel == TREESPEC_KERNEL_TC ? TREESPEC_KERNEL_TC
+        p.kernel = s.kernel == TREESPEC_KERNEL_TC       ? TREESPEC_KERNEL_TC
+                   : s.kernel == TREESPEC_KERNEL_TC_2SM ? TREESPEC_KERNEL_TC_2SM
                    : (s.kernel == TREESPEC_KERNEL_TC_PAIR || paired) ? TREESPEC_KERNEL_TC_PAIR
                                                                       : TREESPEC_KERNEL_TC;
         p.rows_per_block = 128;
@@ -100,7 +109,7 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     p.row_blocks = (R + p.rows_per_block - 1) / p.rows_per_block;
     const long long max_tokens = (long long)s.max_pages_per_seq * s.page_size;
     const int tile = 128;                       // split sizes are multiples of every tile size
-    const bool tc = p.kernel == TREESPEC_KERNEL_TC || p.kernel == TREESPEC_KERNEL_TC_PAIR;
+    const bool tc = p.kernel != TREESPEC_KERNEL_SIMT;
     const long long units = (long long)s.batch * s.num_kv_heads *
                             (p.kernel == TREESPEC_KERNEL_TC_PAIR ? p.row_blocks / 2 : p.row_blocks);
     long long splits;
@@ -263,9 +272,10 @@ extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* 
     if (launch_tree_prologue(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches++;
     const cudaError_t e = plan.kernel == TREESPEC_KERNEL_TC_PAIR ? launch_attn_tc_pair(p, st)
+                          : plan.kernel == TREESPEC_KERNEL_TC_2SM ? launch_attn_tc_2sm(p, st)
                           : plan.kernel == TREESPEC_KERNEL_TC    ? launch_attn_tc(p, st)
                                                                  : launch_attn_simt(p, s.dtype, st);
-    if (e != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    if (e != cudaSuccess) return launch_failed(e);
     g_launches++;
     if (plan.merge) {
         if (launch_attn_merge(p, s.dtype, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
@@ -490,3 +500,9 @@ extern "C" int treespec_version(void) { return 100; }
 extern "C" uint64_t treespec_launch_count(void) { return g_launches.load(); }
 
 extern "C" void treespec_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : kDefaultWaitNs); }
+
+extern "C" int treespec_last_launch_error(const char** name) {
+    const int e = g_launch_error.load();
+    if (name) *name = cudaGetErrorName(cudaError_t(e));
+    return e;
+}

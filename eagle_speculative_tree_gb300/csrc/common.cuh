@@ -68,7 +68,7 @@ struct AttnLayout {
 };
 
 struct AttnPlan {
-    int kernel;          // TREESPEC_KERNEL_SIMT / _TC / _TC_PAIR
+    int kernel;          // TREESPEC_KERNEL_SIMT / _TC / _TC_PAIR / _TC_2SM
     int num_splits;
     int split_tokens;
     int rows_per_block;
@@ -124,6 +124,7 @@ struct AcceptParams {
 cudaError_t launch_tree_prologue(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_tc_2sm(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s);
 bool attn_tc_supported(int dtype, int D);
 // TMA map of a K or V page pool [P][16][Hkv][128] bf16, one page x 64 head dims per box

@@ -63,8 +63,10 @@ enum treespec_kernel {
     TREESPEC_KERNEL_SIMT = 1,  /* CUDA-core split-KV kernel (any dtype) */
     TREESPEC_KERNEL_TC = 2,    /* tcgen05/TMA split-KV kernel (bf16, head_dim 128), one 128-row query tile per CTA */
     TREESPEC_KERNEL_TC_PAIR = 3,  /* the same with two 128-row query tiles per CTA (bf16, head_dim 128, an even
-                                     number of 128-row blocks ceil(N*G / 128)); the automatic choice whenever the
-                                     row blocks pair up */
+                                     number of 128-row blocks ceil(N*G / 128)) */
+    TREESPEC_KERNEL_TC_2SM = 4,   /* tcgen05/TMA split-KV kernel whose MMAs span a pair of CTAs (cta_group::2):
+                                     two 128-row blocks per cluster of two SMs, each SM copying half of every K/V
+                                     tile (bf16, head_dim 128, an even number of 128-row blocks) */
 };
 
 enum treespec_accept_mode {
@@ -112,7 +114,7 @@ typedef struct {
 } treespec_attn_shape;
 
 typedef struct {
-    int32_t kernel;             /* the kernel the call will run (SIMT, TC or TC_PAIR) */
+    int32_t kernel;             /* the kernel the call will run (SIMT, TC, TC_PAIR or TC_2SM) */
     int32_t num_splits;         /* KV splits per (sequence, kv head, row block or pair of them) */
     int32_t split_tokens;       /* logical tokens per split (a multiple of the tile) */
     int32_t rows_per_block;     /* query rows (node x group) one CTA holds */
@@ -353,6 +355,11 @@ const char *treespec_error_string(int code);
 
 /* Library version as major * 10000 + minor * 100 + patch. */
 int treespec_version(void);
+
+/* The CUDA runtime's error code (a cudaError_t; 0 if none) behind the most recent
+ * TREESPEC_ERR_LAUNCH of tree_attn_verify in this process, and its name in *name when
+ * name is not NULL. */
+int treespec_last_launch_error(const char **name);
 
 /* Kernels this process has launched through the library so far (all entry points). */
 uint64_t treespec_launch_count(void);

@@ -47,6 +47,7 @@ def shape(**kw):
     dict(page_size=32), dict(batch=0), dict(dtype=7), dict(max_pages_per_seq=0),
     dict(num_splits=-1), dict(kernel=9),
     dict(kernel=3),                       # two-tile kernel: 8 nodes x 4 query heads is one 128-row block
+    dict(kernel=4),                       # CTA-pair kernel: the same
 ])
 def test_attention_rejects_bad_shapes(kw):
     prob = shape(**kw)

@@ -41,7 +41,7 @@ def row_blocks(w):
     return -(-w.num_nodes * w.group // 128)
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3])
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("name,batch", SMALL)
 def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
     w = gen.get(name)
@@ -49,8 +49,8 @@ def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
         w = w.with_batch(batch)
     if kernel >= 2 and w.dtype != "bf16":
         pytest.skip("the tensor-core kernels take bf16")
-    if kernel == 3 and row_blocks(w) % 2:
-        pytest.skip("the two-tile kernel needs an even number of 128-row blocks")
+    if kernel in (3, 4) and row_blocks(w) % 2:
+        pytest.skip("the two-tile and CTA-pair kernels need an even number of 128-row blocks")
     x = gi.make_inputs(w, with_accept=False)
     out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
@@ -66,7 +66,7 @@ def test_auto_plan_picks_tensor_cores_for_bf16_head128(ts, cuda_device):
         assert ts.attn_plan(prob).kernel == want, name
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("splits", [1, 3, 40])
 def test_split_counts(ts, cuda_device, kernel, splits):
     w = gen.get("c2_llama3_8b_bf16_greedy") if kernel < 3 else gen.get("c4_llama3_70b_bf16_greedy").with_batch(1)
@@ -87,7 +87,7 @@ def _custom(name, parents, prefix, batch=None):
 
 @pytest.mark.parametrize("dtype_cfg,kernel", [("c1_tiny_f32_greedy", 1), ("c2_llama3_8b_bf16_greedy", 1),
                                               ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2),
-                                              ("c4_llama3_70b_bf16_greedy", 3)])
+                                              ("c4_llama3_70b_bf16_greedy", 3), ("c4_llama3_70b_bf16_greedy", 4)])
 @pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
                                   "random64", "random32", "chain128", "star128", "random128", "random100"])
 def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
@@ -115,8 +115,8 @@ def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
     else:
         parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
     w, x = _custom(dtype_cfg, parents, prefix)
-    if kernel == 3 and row_blocks(w) % 2:
-        pytest.skip("the two-tile kernel needs an even number of 128-row blocks")
+    if kernel in (3, 4) and row_blocks(w) % 2:
+        pytest.skip("the two-tile and CTA-pair kernels need an even number of 128-row blocks")
     out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
 
@@ -229,7 +229,7 @@ def test_two_tile_kernel_refuses_an_odd_number_of_row_blocks(ts, cuda_device):
         run(ts, x, cuda_device, kernel=ts.KERNEL_TC_PAIR)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 def test_full_size_every_kernel_on_sampled_pairs(ts, cuda_device, kernel):
     """Every attention kernel on the full bench workload, checked on sampled pairs."""
     w = gen.get("c4_llama3_70b_bf16_greedy")
@@ -242,7 +242,7 @@ def test_full_size_every_kernel_on_sampled_pairs(ts, cuda_device, kernel):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("kernel", [2, 3])
+@pytest.mark.parametrize("kernel", [2, 3, 4])
 @pytest.mark.parametrize("splits", [1, 0])
 def test_tensor_core_kernels_flag_bad_lengths_and_pages(ts, cuda_device, kernel, splits):
     """An invalid sequence gets zero rows (written by the kernel itself with one split, by
