@@ -90,17 +90,24 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
                        (long long)s.num_pool_pages * s.page_size < (1ll << 31);
     // Tensor cores for every bf16 / head_dim 128 shape: measured faster than the CUDA-core
     // kernel from 16 rows per kv head up (rows are padded to the 128-row MMA tile).
-    // The two-tile kernel wherever the row blocks of a kv head pair up: one CTA then reads
-    // each K/V tile for 256 query rows, the one-tile kernel for 128, and the L2 reads of the
-    // one-tile kernel bind first (32 x 8192 tokens, 64 q / 8 kv heads, 64 nodes: 0.471 ms
-    // against 0.541 at batch 32, 0.244 against 0.317 at batch 16).
+    // Where the row blocks of a kv head pair up, a K/V tile should serve 256 rows: the
+    // one-tile kernel's L2 reads bind first otherwise.  Of the two kernels that do that, the
+    // CTA-pair kernel (256-row MMAs across two SMs) when the two-tile kernel's CTAs would
+    // not fill the SMs once, the two-tile kernel (two 128-row tiles in one CTA) otherwise.
+    // Measured at 64 q / 8 kv heads, 64 nodes, 8192-token prefixes (ms, CTA pair / two-tile /
+    // one-tile): batch 2 0.080 / 0.088 / -, batch 8 0.149 / 0.169 / 0.169, batch 16
+    // 0.279 / 0.243 / 0.315, batch 32 0.491 / 0.474 / 0.543.
     if (s.kernel == TREESPEC_KERNEL_TC || s.kernel == TREESPEC_KERNEL_TC_PAIR || s.kernel == TREESPEC_KERNEL_TC_2SM ||
         (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
-        const bool paired = ((R + 127) / 128) % 2 == 0;
+        const long long rbs = (R + 127) / 128;
+        const bool paired = rbs % 2 == 0;
+        const bool small = (long long)s.batch * s.num_kv_heads * (rbs / 2) < sms;
         p.kernel = s.kernel == TREESPEC_KERNEL_TC       ? TREESPEC_KERNEL_TC
                    : s.kernel == TREESPEC_KERNEL_TC_2SM ? TREESPEC_KERNEL_TC_2SM
-                   : (s.kernel == TREESPEC_KERNEL_TC_PAIR || paired) ? TREESPEC_KERNEL_TC_PAIR
-                                                                      : TREESPEC_KERNEL_TC;
+                   : s.kernel == TREESPEC_KERNEL_TC_PAIR ? TREESPEC_KERNEL_TC_PAIR
+                   : !paired                             ? TREESPEC_KERNEL_TC
+                   : small                               ? TREESPEC_KERNEL_TC_2SM
+                                                         : TREESPEC_KERNEL_TC_PAIR;
         p.rows_per_block = 128;
     } else {
         p.kernel = TREESPEC_KERNEL_SIMT;

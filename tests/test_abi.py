@@ -82,10 +82,12 @@ def test_plan_and_workspace_query():
 def test_plan_pairs_query_tiles_when_the_row_blocks_pair_up():
     """Without a device the planner assumes 152 SMs."""
     wide = dict(num_nodes=64, num_q_heads=64, num_kv_heads=8)      # 512 rows: four 128-row blocks
-    b8 = ts.attn_plan(shape(batch=8, **wide))
-    assert b8.kernel == ts.KERNEL_TC_PAIR and b8.rows_per_block == 128 and b8.row_blocks == 4
-    assert ts.attn_plan(shape(batch=32, **wide)).kernel == ts.KERNEL_TC_PAIR
-    assert ts.attn_plan(shape(batch=1, **wide)).kernel == ts.KERNEL_TC_PAIR
+    b8 = ts.attn_plan(shape(batch=8, **wide))                      # 128 two-tile CTAs: under one wave
+    assert b8.kernel == ts.KERNEL_TC_2SM and b8.rows_per_block == 128 and b8.row_blocks == 4
+    assert ts.attn_plan(shape(batch=32, **wide)).kernel == ts.KERNEL_TC_PAIR    # 512 two-tile CTAs
+    assert ts.attn_plan(shape(batch=10, **wide)).kernel == ts.KERNEL_TC_PAIR    # 160 two-tile CTAs: a wave and more
+    assert ts.attn_plan(shape(batch=9, **wide)).kernel == ts.KERNEL_TC_2SM      # 144: under one wave
+    assert ts.attn_plan(shape(batch=1, **wide)).kernel == ts.KERNEL_TC_2SM
     assert ts.attn_plan(shape(batch=8, kernel=ts.KERNEL_TC, **wide)).kernel == ts.KERNEL_TC
     assert ts.attn_plan(shape(batch=32, kernel=ts.KERNEL_TC_PAIR, **wide)).kernel == ts.KERNEL_TC_PAIR
     assert ts.attn_plan(shape(batch=8, num_nodes=40, num_q_heads=64, num_kv_heads=8)).kernel == ts.KERNEL_TC

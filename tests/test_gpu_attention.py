@@ -185,15 +185,15 @@ def test_full_size_bench_workload_sampled(ts, cuda_device):
 
 
 def test_batch8_automatic_plan_in_full(ts, cuda_device):
-    """The Llama-3-70B shape at batch 8 through the automatic plan (two-tile kernel, KV
-    split in two, merge), every (sequence, kv head) pair against the oracle."""
+    """The Llama-3-70B shape at batch 8 through the automatic plan (the CTA-pair kernel),
+    every (sequence, kv head) pair against the oracle."""
     from oracle_pool import oracle_attention_pairs
     name = "c4_llama3_70b_bf16_greedy@b8"
     w = gen.get(name)
     x = gi.make_inputs(w, with_accept=False)
     d = attn_device_inputs(x, cuda_device)
     plan = ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"]))
-    assert plan.kernel == ts.KERNEL_TC_PAIR and plan.merge
+    assert plan.kernel == ts.KERNEL_TC_2SM
     out = run(ts, x, cuda_device)
     pairs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
     ref = oracle_attention_pairs(name, pairs, workers=16)
