@@ -6,9 +6,9 @@
 // + g) and one split of the sequence's logical tokens, in 64-token KV tiles:
 //   * shared memory: Q of both query tiles (written once by the softmax warps, 128-byte
 //     swizzle), a five-stage K ring (warp 8) and a five-stage V ring (warp 9) filled by
-//     TMA one 16-token page x 64 head dims per copy; the partly filled last page of a
-//     sequence and pages past the split are written by the producer warp itself,
-//     zero-filled;
+//     TMA one 16-token page x 64 head dims per copy (the page producer shared with the
+//     other tensor-core kernels: the partly filled last page of a sequence and pages
+//     past the split are written by the producer warp itself, zero-filled);
 //   * TMEM (all 512 columns): for each query tile t two 64-column S buffers and O_t;
 //     P_t(j) is written over the first 32 columns of S buffer j % 2 as packed bf16;
 //   * warp 10 issues the MMAs of query tile 0 and warp 11 those of tile 1, in the order
@@ -24,22 +24,18 @@
 //     more than 2^8 (after P_t(j-1) V(j-1) has completed), and write P back to TMEM.
 // Every mbarrier wait is bounded; on expiry the CTA records TREESPEC_STATUS_TIMEOUT,
 // drains its own tensor-core work, frees TMEM and exits.
-#include <cuda.h>
-
-#include "common.cuh"
-#include "sm100.cuh"
+#include "attn_tc_parts.cuh"
 
 namespace treespec {
 
 namespace {
 
 using namespace sm100;
+using tcparts::kD;                   // head dim
 
 constexpr int kM = 128;              // query rows per tile = TMEM lanes
 constexpr int kNQ = 2;               // query tiles per CTA
-constexpr int kD = 128;              // head dim
 constexpr int kBN = 64;              // tokens per KV tile
-constexpr int kPages = kBN / 16;     // 16-token pages per KV tile
 constexpr int kNSK = 5;              // K ring stages
 constexpr int kNSV = 5;              // V ring stages
 constexpr int kQPanel = kM * 128;    // one [128 rows][64 bf16] swizzled panel of Q, bytes
@@ -72,7 +68,7 @@ struct Bars {
 };
 constexpr int kOffMisc = kOffBar + int(sizeof(Bars));
 constexpr int kOffAnc = kOffMisc + 16;
-constexpr int kSmemBytes = kOffAnc + kMaxNodes * kAncWords * 8;         // 231,744 bytes
+constexpr int kSmemBytes = kOffAnc + kMaxNodes * kAncWords * 8;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -93,16 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = p.lens[b];
 
     if (S < 0) {                                   // invalid sequence: zeros (or the merge writes them)
-        if (!p.merge && split == 0) {
-            for (int e = tid; e < kNQ * kM * (kD / 8); e += kThreads) {
-                const int row = r0 + e / (kD / 8), c = e % (kD / 8);
-                if (row >= p.R) continue;
-                const int i = row / p.G, hq = h * p.G + row % p.G;
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                      ((size_t(b) * p.N + i) * p.Hq + hq) * kD) + c;
-                *dst = make_uint4(0, 0, 0, 0);
-            }
-        }
+        if (!p.merge && split == 0) tcparts::zero_rows(p, b, h, r0, kNQ * kM, kThreads);
         return;
     }
     const int nb = p.nn[b];                        // rows of nodes nb.. are padding: zero output
@@ -154,89 +141,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == kWarpK || warp == kWarpV) {
         // ------------------------------------------------------------ TMA producers
         const bool is_v = warp == kWarpV;
-        const int nst = is_v ? kNSV : kNSK;
-        uint64_t* full = is_v ? bars->v_full : bars->k_full;
-        uint64_t* empty = is_v ? bars->v_empty : bars->k_empty;
-        const uint16_t* src = static_cast<const uint16_t*>(is_v ? p.v : p.k);
-        const CUtensorMap* map = is_v ? &tmv : &tmk;
-        unsigned char* ring = sm + (is_v ? kOffV : kOffK);
-        const int* ptab = p.page_table + size_t(b) * p.max_pages;
-        if (lane == 0) tma_prefetch_desc(map);
-        // page ids in batches of eight tiles (lane l: page l & 3 of tile 8 * batch + (l >> 2)),
-        // fetched a batch ahead
-        auto fetch_batch = [&](int bi) -> int {
-            const int jt = 8 * bi + (lane >> 2);
-            const int pos0 = t0 + jt * kBN + (lane & 3) * 16;
-            return (jt < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
-        };
-        int batch_cur = fetch_batch(0), batch_next = fetch_batch(1);
-        int armed = 0;                                      // tiles whose stage this warp armed
-        for (int j = 0; j < ntiles; ++j) {
-            const int stage = j % nst;
-            if (j > 0 && (j & 7) == 0) {
-                batch_cur = batch_next;
-                batch_next = fetch_batch((j >> 3) + 1);
-            }
-            int page = __shfl_sync(0xffffffffu, batch_cur, ((j & 7) << 2) | (lane & 3));
-            const int base = t0 + j * kBN;
-            // lanes 0..3 own page `lane` of the tile: 1 = full page by TMA, 2 = written here
-            const int pos0 = base + lane * 16;
-            int kind = 0;
-            if (lane < kPages) {
-                kind = 2;
-                if (pos0 < t1) {
-                    const bool ok = page >= 0 && page < p.num_pool_pages;
-                    if (!ok) atomicOr(p.status, TREESPEC_STATUS_BAD_PAGE);
-                    if (ok && pos0 + 16 <= L) kind = 1;
-                    if (!ok) page = -1;
-                } else {
-                    page = -1;
-                }
-            }
-            if (j >= nst && !mbar_wait_bounded(&empty[stage], ((j / nst) - 1) & 1, p.wait_ns)) {
-                *abort_flag = 1;
-                atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
-            }
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            unsigned char* dst = ring + stage * kTile;
-            const unsigned manual = __ballot_sync(0xffffffffu, kind == 2);
-            if (manual) {
-                for (int pg = 0; pg < kPages; ++pg) {
-                    if (!((manual >> pg) & 1u)) continue;
-                    const int pgid = __shfl_sync(0xffffffffu, page, pg);
-                    const int q0 = base + pg * 16;
-                    for (int c = lane; c < 16 * 16; c += 32) {      // 16 token rows x 16 chunks of 16 bytes
-                        const int rr = c >> 4, ch = c & 15;
-                        const int pos = q0 + rr;
-                        uint4 val = make_uint4(0, 0, 0, 0);
-                        if (pgid >= 0 && pos < t1) {
-                            const size_t off = ((size_t(pgid) * p.ps + (pos & 15)) * p.Hkv + h) * kD + ch * 8;
-                            val = __ldg(reinterpret_cast<const uint4*>(src + off));
-                        }
-                        *reinterpret_cast<uint4*>(dst + (ch >> 3) * kPanel + sw128_offset(pg * 16 + rr, ch & 7)) = val;
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            const unsigned viatma = __ballot_sync(0xffffffffu, kind == 1);
-            if (lane == 0) mbar_arrive_expect_tx(&full[stage], uint32_t(__popc(viatma)) * 2u * 2048u);
-            __syncwarp();
-            if (kind == 1) {                                 // each page's two copies
-                const int z = page * 16;
-                tma_load_3d(dst + lane * 2048, map, 0, h, z, &full[stage]);
-                tma_load_3d(dst + kPanel + lane * 2048, map, 64, h, z, &full[stage]);
-            }
-            __syncwarp();
-            ++armed;
-        }
-        // Every copy this warp started has landed before the CTA may end: after an abort the
-        // consumers no longer wait for them.  The last phase armed on each stage completes
-        // once its copies arrive (earlier phases completed before it was armed).
-        for (int s2 = 0; s2 < nst && s2 < armed; ++s2) {
-            const int last = s2 + ((armed - 1 - s2) / nst) * nst;
-            mbar_wait_bounded(&full[s2], uint32_t(last / nst) & 1u, kDefaultWaitNs);
-        }
+        tcparts::ProducerArgs a;
+        a.map = is_v ? &tmv : &tmk;
+        a.src = static_cast<const uint16_t*>(is_v ? p.v : p.k);
+        a.ring = sm + (is_v ? kOffV : kOffK);
+        a.full = is_v ? bars->v_full : bars->k_full;
+        a.empty = is_v ? bars->v_empty : bars->k_empty;
+        a.nst = is_v ? kNSV : kNSK;
+        a.stage_bytes = kTile;
+        a.panel_bytes = kPanel;
+        a.pg0 = 0;
+        a.npg = kBN / 16;
+        a.dp0 = 0;
+        a.ndp = 2;
+        tcparts::produce_pages<kBN>(p, a, b, h, t0, t1, L, ntiles, abort_flag);
       } else {
         // ------------------------------------------------------------ MMA issuers
         // Warp 10 + t issues every MMA of tile t.  The whole warp runs the loop (all lanes
@@ -344,25 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool alive = true;
         uint32_t v[kBN];
         for (int j = 0; j < ntiles; ++j) {
-            const int base = t0 + j * kBN;
             const int bf = j & 1;
             const uint32_t scol = scol0 + bf * 64u;
-            // which of the tile's columns the row may see, as 32-bit words: prefix columns
-            // below pref_end, tree columns [tree_lo, tree_hi) via the ancestor word
-            const int pref_end = min(S, t1) - base;
-            const int tree_lo = S - base, tree_hi = t1 - base;
             uint32_t mw[kBN / 32];
-#pragma unroll
-            for (int w = 0; w < kBN / 32; ++w) {
-                const int lo = 32 * w;
-                const int np = min(max(pref_end - lo, 0), 32);
-                uint32_t bits = np == 32 ? 0xffffffffu : ((1u << np) - 1u);
-                const int nh = min(max(tree_hi - lo, 0), 32);
-                const uint32_t hi_mask = nh == 32 ? 0xffffffffu : ((1u << nh) - 1u);
-                const uint32_t tb = anc_bits32(anc0, anc1, lo - tree_lo);   // set bit of column lo: lo - tree_lo
-                bits |= tb & hi_mask;
-                mw[w] = row_ok ? bits : 0u;
-            }
+            tcparts::tile_mask<kBN>(mw, t0 + j * kBN, S, t1, anc0, anc1, row_ok);
             const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
             if (!mbar_wait_bounded(&bars->s_full[t][bf], (j >> 1) & 1, p.wait_ns)) { alive = false; break; }
             tc_fence_after();
@@ -371,41 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBN / 32; ++c) tmem_ld32(scol + c * 32, v + c * 32);
                 tmem_wait_ld();
             }
-            if (!full) {
-                constexpr uint32_t kNegInf = 0xff800000u;
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
-            }
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < kBN; c += 8) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    mx[e] = fmax3(mx[e], __uint_as_float(v[c + 2 * e]), __uint_as_float(v[c + 2 * e + 1]));
-            }
-            const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sc;   // scale > 0 commutes with max
-            bool resc = false;
-            float alpha = 1.f;
-            if (mt > m_used + 8.f) {
-                alpha = ex2(m_used - mt);
-                resc = m_used != -INFINITY;
-                l *= alpha;
-                m_used = mt;
-            }
-            // probabilities 2^(s*scale - m_used), rounded to bf16 and packed in pairs in place
-            // (pair c overwrites v[c], whose value was read at pair c/2)
-            const float msub = m_used == -INFINITY ? 0.f : m_used;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBN / 2; ++c) {
-                float x0, x1;
-                fma_f32x2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), sc, -msub);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                v[c] = pack_bf16x2(p0, p1);
-                if (c & 1) add_f32x2(a2, a3, p0, p1);
-                else add_f32x2(a0, a1, p0, p1);
-            }
-            l += (a0 + a1) + (a2 + a3);
+            bool resc;
+            float alpha;
+            tcparts::softmax_tile<kBN>(v, mw, full, sc, m_used, l, resc, alpha);
             if (warp_rows) tmem_st32(scol, v);             // P over the first 32 columns of the buffer
             tmem_wait_st();
             if (__any_sync(0xffffffffu, resc)) {
@@ -415,17 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float f = resc ? alpha : 1.f;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(ocol + c * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st32(ocol + c * 32, o);
-                    tmem_wait_st();                        // frees o[] before the next chunk
-                }
+                tcparts::rescale_o(ocol, resc ? alpha : 1.f);
             }
             tc_fence_before();
             mbar_arrive(&bars->p_full[t][bf]);
@@ -435,50 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
         } else {
             tc_fence_after();
-            const float inv = 1.f / l;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                if (warp_rows) {
-                    tmem_ld32(ocol + c * 32, o);
-                    tmem_wait_ld();
-                }
-                const int col0 = c * 32;
-                if (!row_ok) {
-                    if (row_in && !p.merge) {                // padding slot: zeros (the merge writes them otherwise)
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                              ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(0, 0, 0, 0);
-                    }
-                    continue;
-                }
-                if (!p.merge) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                          ((size_t(b) * p.N + i) * p.Hq + hq) * kD + col0);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int k2 = 0; k2 < 4; ++k2) {
-                            const int idx = e * 8 + k2 * 2;
-                            w4[k2] = pack_bf16x2(__uint_as_float(o[idx]) * inv, __uint_as_float(o[idx + 1]) * inv);
-                        }
-                        dst[e] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
-                } else {
-                    const size_t prow = (size_t(b * p.Hkv + h) * p.num_splits + split) * p.R + r;
-                    float4* dst = reinterpret_cast<float4*>(p.part_acc + prow * kD + col0);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                             __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-                    if (c == 0) {
-                        p.part_ml[prow * 2] = m_used;
-                        p.part_ml[prow * 2 + 1] = l;
-                    }
-                }
-            }
+            tcparts::write_row(p, ocol, warp_rows, row_in, row_ok, b, i, hq, h, split, r, m_used, l);
         }
     }
 
