@@ -292,7 +292,7 @@ def run_gpu(args):
              par=t(x.tree_parents), lg=t(x.target_logits), tok=t(x.draft_tokens),
              qp=None if w.greedy else t(x.draft_probs), u=None if w.greedy else t(x.uniforms))
     out = torch.empty_like(d["q"])
-    prob = ts.attn_problem(d["q"], d["k"], d["pt"], kernel=args.attn_kernel)
+    prob = ts.attn_problem(d["q"], d["k"], d["pt"], kernel=args.attn_kernel, num_splits=args.attn_splits)
     plan = ts.attn_plan(prob)
     ws_a = torch.empty(ts.attn_workspace_bytes(prob), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(ts.accept_workspace_bytes(w.batch, w.num_nodes, w.vocab), dtype=torch.uint8, device=dev)
@@ -303,7 +303,7 @@ def run_gpu(args):
 
     def step(inp):
         ts.tree_attn_verify(inp["q"], d["k"], d["v"], inp["pt"], inp["pl"], inp["par"], out,
-                            kernel=args.attn_kernel, workspace=ws_a, stream=stream)
+                            kernel=args.attn_kernel, num_splits=args.attn_splits, workspace=ws_a, stream=stream)
         ts.tree_accept(inp["lg"], inp["tok"], inp["qp"], inp["par"], inp["u"], w.temperature,
                        accept_path=path, accept_len=alen, bonus_token=bonus, mode=args.accept_mode,
                        workspace=ws_b, stream=stream)
@@ -331,7 +331,7 @@ def run_gpu(args):
     for i in range(K):
         ev[i][0].record(stream)
         ts.tree_attn_verify(resident["q"], d["k"], d["v"], resident["pt"], resident["pl"], resident["par"], out,
-                            kernel=args.attn_kernel, workspace=ws_a, stream=stream)
+                            kernel=args.attn_kernel, num_splits=args.attn_splits, workspace=ws_a, stream=stream)
         ev[i][1].record(stream)
         ts.tree_accept(resident["lg"], resident["tok"], resident["qp"], resident["par"], resident["u"],
                        w.temperature, accept_path=path, accept_len=alen, bonus_token=bonus, mode=args.accept_mode,
@@ -391,7 +391,7 @@ def run_gpu(args):
         stream.wait_event(drained[i])                        # its results buffer has been read out
         inp, res = dsts[i], outs[i]
         ts.tree_attn_verify(inp["q"], d["k"], d["v"], inp["pt"], inp["pl"], inp["par"], res["out"],
-                            kernel=args.attn_kernel, workspace=ws_a, stream=stream)
+                            kernel=args.attn_kernel, num_splits=args.attn_splits, workspace=ws_a, stream=stream)
         ts.tree_accept(inp["lg"], inp["tok"], inp["qp"], inp["par"], inp["u"], w.temperature,
                        accept_path=res["path"], accept_len=res["alen"], bonus_token=res["bonus"],
                        mode=args.accept_mode, workspace=ws_b, stream=stream)
@@ -640,7 +640,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS) +
                     [f"{n}@b{b}" for n in gen.WORKLOADS for b in (1, 2, 8, 16, 32, 64)])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--attn-kernel", type=int, default=0, help="0 auto, 1 CUDA cores, 2 tensor cores")
+    ap.add_argument("--attn-kernel", type=int, default=0,
+                    help="0 auto, 1 CUDA cores, 2 tensor cores, 3 two query tiles per CTA, 4 CTA pairs")
+    ap.add_argument("--attn-splits", type=int, default=0, help="KV splits per (sequence, kv head); 0 = planner")
     ap.add_argument("--accept-mode", type=int, default=0, help="0 auto, 1 all rows, 2 path only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep (1 GPU only)")
