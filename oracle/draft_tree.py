@@ -21,15 +21,22 @@ Readings where the pages are silent (the CUDA entry points follow the same ones)
     decides in, so both sides rank identically;
   * the rerank keeps the root and the N - 1 non-root nodes with the highest score, ties
     to the lower node index, numbered in increasing original index (a topological order,
-    since a node's parent was added before it).  All scored candidates are eligible, so
-    a tree may be larger than steps * k nodes.  A kept node whose parent was dropped
-    (only possible with positive log-probabilities) is attached to the root and flagged.
+    since a node's parent was added before it).  By default all scored candidates are
+    eligible, so a tree may be larger than steps * k nodes; a caller may instead name the
+    eligible nodes (a pool), e.g. only the nodes that entered some step's beam -- the
+    reading under which a 5-step, top-4 expansion reranks 20 candidates.  A kept node
+    whose parent was dropped (only possible with positive log-probabilities, or a pool
+    that omits a kept node's parent) is attached to the root and flagged.  A pool with
+    fewer than N - 1 eligible nodes gives a smaller tree: its row is padded after the last
+    kept node with parent ABSENT (-2) and token -1, the layout of a batch that mixes tree
+    sizes.
 """
 from __future__ import annotations
 
 import numpy as np
 
 BAD_PARENT = 1
+ABSENT = -2       # parent entry of a padding slot after a smaller tree
 
 
 def step_base(step: int, topk: int) -> int:
@@ -71,16 +78,20 @@ def draft_step(logprobs: np.ndarray, frontier: np.ndarray, node_parent: np.ndarr
     return nxt
 
 
-def rerank(node_parent: np.ndarray, node_token: np.ndarray, node_score: np.ndarray, num_nodes: int):
-    """Returns (parents [B][N], tokens [B][N], status)."""
+def rerank(node_parent: np.ndarray, node_token: np.ndarray, node_score: np.ndarray, num_nodes: int,
+           pool: np.ndarray | None = None):
+    """Returns (parents [B][N], tokens [B][N], status).  pool [B][P] (node ids) restricts the
+    eligible non-root nodes; None makes every node 1 .. M-1 eligible."""
     B, M = node_parent.shape
     N = num_nodes
     parents = np.full((B, N), -1, dtype=np.int32)
     tokens = np.full((B, N), -1, dtype=np.int32)
     status = 0
     for b in range(B):
-        ranked = sorted(range(1, M), key=lambda i: (-float(np.float32(node_score[b, i])), i))
+        eligible = range(1, M) if pool is None else sorted({int(i) for i in pool[b] if 0 < int(i) < M})
+        ranked = sorted(eligible, key=lambda i: (-float(np.float32(node_score[b, i])), i))
         kept = sorted(ranked[:N - 1])
+        parents[b, 1 + len(kept):] = ABSENT
         new = {0: 0}
         for j, i in enumerate(kept):
             new[i] = j + 1

@@ -130,3 +130,63 @@ def test_planted_reversed_ranking_fails_the_brute_force():
     pairs = [(np.float32(sc[0, n] + lp1[0, f, v]), f, v) for f, n in enumerate(frontier) for v in range(7)]
     best = sorted(pairs, key=lambda t: (-float(t[0]), t[1], t[2]))[:3]
     assert [(int(par[0, n]), int(tok[0, n])) for n in f1[0]] != [(frontier[f], v) for _s, f, v in best]
+
+
+def replay_generator_tree(rng, steps, k, n):
+    """The draft steps and rerank of this oracle fed the generator's own draws: each
+    expanded node's children get the next sorted top-k log-probabilities from `rng`, drawn
+    in frontier order (best first), as gen.trees.build_tree draws them.  The rerank takes
+    the beam nodes when steps * k >= n - 1 (the generator's candidate set then) and every
+    candidate otherwise.  Returns the reranked parent array."""
+    from gen import trees
+    M = odt.num_nodes_after(steps, k)
+    par = np.zeros((1, M), np.int32)
+    tok = np.zeros((1, M), np.int32)
+    sc = np.zeros((1, M), np.float32)
+    front = np.zeros((1, 1), np.int32)
+    beam = []
+    for s in range(steps):
+        F = 1 if s == 0 else k
+        rows = np.stack([trees._child_logprobs(rng, k) for _ in range(F)]).astype(np.float32)[None]
+        front = odt.draft_step(rows, front, par, tok, sc, s, k)
+        beam.extend(front[0].tolist())
+    pool = np.asarray([beam]) if steps * k >= n - 1 else None
+    parents, _tokens, status = odt.rerank(par, tok, sc, n, pool=pool)
+    assert status == 0
+    return parents[0]
+
+
+@pytest.mark.parametrize("name", ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy", "c3_llama2_7b_bf16_stoch",
+                                  "c4_llama3_70b_bf16_greedy", "c5_ragged_b64_bf16_stoch"])
+def test_steps_and_rerank_rebuild_the_generator_trees(name):
+    """The generator (gen/trees.py) and this oracle state the same drafting reading in code
+    of their own (float64 sums there, float32 here): on every workload's seeded tree
+    recipe they must produce the same parent arrays, including the 20-candidate beam
+    rerank of the 5-step, top-4 recipe."""
+    import gen
+    from gen import inputs as gi, trees
+    w = gen.get(name)
+    for b in range(min(w.batch, 8) if w.vary_tree else 1):
+        want = trees.build_tree(gi.rng_for(w, b, gi.TREE), w.num_steps, w.topk, w.num_nodes)
+        got = replay_generator_tree(gi.rng_for(w, b, gi.TREE), w.num_steps, w.topk, w.num_nodes)
+        assert np.array_equal(got, want), (name, b)
+
+
+def test_pool_restricts_the_rerank():
+    # a chain of beam picks: with the pool {1, 4} only those two can be kept; with no pool
+    # the best two of all nodes
+    par = np.array([[-1, 0, 0, 1, 1]], np.int32)
+    tok = np.array([[-1, 10, 11, 12, 13]], np.int32)
+    sc = np.array([[0, -1.0, -0.5, -3.0, -2.0]], np.float32)
+    p_all, t_all, st = odt.rerank(par, tok, sc, 3)
+    assert st == 0 and t_all[0].tolist() == [-1, 10, 11]
+    p_pool, t_pool, st = odt.rerank(par, tok, sc, 3, pool=np.array([[1, 4]]))
+    assert st == 0 and t_pool[0].tolist() == [-1, 10, 13] and p_pool[0].tolist() == [-1, 0, 1]
+
+
+def test_small_pool_pads_the_tree():
+    par = np.array([[-1, 0, 0, 1]], np.int32)
+    tok = np.array([[-1, 10, 11, 12]], np.int32)
+    sc = np.array([[0, -1.0, -0.5, -3.0]], np.float32)
+    p, t, st = odt.rerank(par, tok, sc, 4, pool=np.array([[2]]))
+    assert st == 0 and p[0].tolist() == [-1, 0, odt.ABSENT, odt.ABSENT] and t[0].tolist() == [-1, 11, -1, -1]
