@@ -68,6 +68,8 @@ _lib.tree_draft_step.argtypes = [_vp] + [ctypes.c_int32] * 5 + [_vp] * 4 + [ctyp
 _lib.tree_draft_step.restype = ctypes.c_int
 _lib.tree_rerank.argtypes = [_vp] * 3 + [ctypes.c_int32] * 3 + [_vp] * 3 + [ctypes.c_size_t, _vp]
 _lib.tree_rerank.restype = ctypes.c_int
+_lib.tree_rerank_pool.argtypes = [_vp] * 4 + [ctypes.c_int32] * 4 + [_vp] * 3 + [ctypes.c_size_t, _vp]
+_lib.tree_rerank_pool.restype = ctypes.c_int
 _lib.treespec_read_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
 _lib.treespec_read_status.restype = ctypes.c_int
 _lib.treespec_error_string.argtypes = [ctypes.c_int]
@@ -337,9 +339,10 @@ def tree_draft_step(logprobs, step: int, topk: int, frontier_in, node_parent, no
 
 
 def tree_rerank(node_parent, node_token, node_score, num_nodes: int, tree_parents=None, draft_tokens=None, *,
-                workspace: Optional[torch.Tensor] = None, stream=None):
-    """Keep the root and the num_nodes - 1 best nodes; returns (tree_parents, draft_tokens)
-    [B][num_nodes] int32.  See include/treespec.h."""
+                pool=None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Keep the root and the num_nodes - 1 best nodes (of all, or of `pool` [B][P] int32
+    node ids: tree_rerank_pool); returns (tree_parents, draft_tokens) [B][num_nodes] int32.
+    See include/treespec.h."""
     dev = node_parent.device
     _need(node_parent, "node_parent", torch.int32, dev)
     _need(node_token, "node_token", torch.int32, dev)
@@ -351,9 +354,15 @@ def tree_rerank(node_parent, node_token, node_score, num_nodes: int, tree_parent
         draft_tokens = torch.empty((B, num_nodes), dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = torch.empty(256, dtype=torch.uint8, device=dev)
-    _check(_lib.tree_rerank(_ptr(node_parent), _ptr(node_token), _ptr(node_score), B, M, num_nodes,
-                            _ptr(tree_parents), _ptr(draft_tokens), _ptr(workspace), workspace.numel(),
-                            _stream_handle(stream, dev)))
+    if pool is None:
+        _check(_lib.tree_rerank(_ptr(node_parent), _ptr(node_token), _ptr(node_score), B, M, num_nodes,
+                                _ptr(tree_parents), _ptr(draft_tokens), _ptr(workspace), workspace.numel(),
+                                _stream_handle(stream, dev)))
+    else:
+        _need(pool, "pool", torch.int32, dev)
+        _check(_lib.tree_rerank_pool(_ptr(node_parent), _ptr(node_token), _ptr(node_score), _ptr(pool),
+                                     pool.shape[1], B, M, num_nodes, _ptr(tree_parents), _ptr(draft_tokens),
+                                     _ptr(workspace), workspace.numel(), _stream_handle(stream, dev)))
     return tree_parents, draft_tokens
 
 

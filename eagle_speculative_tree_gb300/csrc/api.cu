@@ -402,7 +402,7 @@ extern "C" int tree_kv_commit(void* k_pages, void* v_pages, const int32_t* page_
 extern "C" size_t treespec_draft_workspace_bytes(int32_t batch, int32_t frontier, int32_t topk) {
     if (batch < 1 || batch > 65535 || frontier < 1 || frontier > kMaxFrontier || topk < 1 || topk > kMaxTopk)
         return 0;
-    const size_t per = size_t(batch) * frontier * topk;
+    const size_t per = size_t(batch) * frontier * kMaxDraftSplits * topk;
     return kWsAlign + align_up(per * 4, kWsAlign) * 2;
 }
 
@@ -425,7 +425,7 @@ extern "C" int tree_draft_step(const float* logprobs, int32_t batch, int32_t fro
     int rc = check_device();
     if (rc != TREESPEC_OK) return rc;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    const size_t per = size_t(batch) * frontier * topk;
+    const size_t per = size_t(batch) * frontier * kMaxDraftSplits * topk;
     DraftParams p{};
     p.logprobs = logprobs;
     p.frontier_in = frontier_in;
@@ -442,6 +442,22 @@ extern "C" int tree_draft_step(const float* logprobs, int32_t batch, int32_t fro
     p.k = topk;
     p.step = step;
     p.M = max_nodes;
+    // A row's vocabulary is cut into S parts (one CTA each) only where the rows alone would
+    // leave SMs idle: each warp's list filters best over a long stream (its k-th entry
+    // rises and fewer groups pass the vote), so parts cost more than they save once every
+    // SM has a row (measured: 64 rows of 8 frontier nodes x 128256 tokens took 58 us per
+    // step in one part, more in three).  No part below 8192 tokens, parts a multiple of
+    // 1024 tokens.
+    {
+        const long long rows = (long long)batch * frontier;
+        long long S = sm_count_or_default() / rows;
+        S = std::min<long long>(S, std::max<long long>(1, vocab / 8192));
+        S = std::max<long long>(1, std::min<long long>(S, kMaxDraftSplits));
+        long long chunk = (vocab + S - 1) / S;
+        chunk = (chunk + 1023) / 1024 * 1024;
+        p.S = int((vocab + chunk - 1) / chunk);
+        p.chunk = int(chunk);
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     if (launch_draft_step(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
@@ -453,7 +469,16 @@ extern "C" int tree_rerank(const int32_t* node_parent, const int32_t* node_token
                            int32_t batch, int32_t max_nodes, int32_t num_nodes, int32_t* tree_parents,
                            int32_t* draft_tokens, void* workspace, size_t workspace_bytes,
                            treespec_stream_t stream) {
+    return tree_rerank_pool(node_parent, node_token, node_score, nullptr, 0, batch, max_nodes, num_nodes,
+                            tree_parents, draft_tokens, workspace, workspace_bytes, stream);
+}
+
+extern "C" int tree_rerank_pool(const int32_t* node_parent, const int32_t* node_token, const float* node_score,
+                                const int32_t* pool, int32_t pool_size, int32_t batch, int32_t max_nodes,
+                                int32_t num_nodes, int32_t* tree_parents, int32_t* draft_tokens, void* workspace,
+                                size_t workspace_bytes, treespec_stream_t stream) {
     if (batch < 1 || batch > 65535 || max_nodes < 1 || max_nodes > kMaxDraftNodes) return TREESPEC_ERR_SHAPE;
+    if (pool ? (pool_size < 1 || pool_size > kMaxDraftNodes) : pool_size != 0) return TREESPEC_ERR_SHAPE;
     if (num_nodes < 1 || num_nodes > kMaxNodes || num_nodes > max_nodes) return TREESPEC_ERR_SHAPE;
     if (!node_parent || !node_token || !node_score || !tree_parents || !draft_tokens)
         return TREESPEC_ERR_NULL_POINTER;
@@ -465,6 +490,8 @@ extern "C" int tree_rerank(const int32_t* node_parent, const int32_t* node_token
     p.node_parent = node_parent;
     p.node_token = node_token;
     p.node_score = node_score;
+    p.pool = pool;
+    p.P = pool_size;
     p.parents = tree_parents;
     p.tokens = draft_tokens;
     p.status = static_cast<uint32_t*>(workspace);

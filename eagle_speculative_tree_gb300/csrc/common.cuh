@@ -150,6 +150,7 @@ cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s);
 constexpr int kMaxTopk = 16;          // branching per step
 constexpr int kMaxFrontier = 16;      // frontier rows per step (1 or topk)
 constexpr int kMaxDraftNodes = 1024;  // node arrays of a sequence (root + steps * topk)
+constexpr int kMaxDraftSplits = 16;   // CTAs that share one frontier row's vocabulary
 struct DraftParams {
     const float* logprobs;            // [B][F][V]
     const int32_t* frontier_in;       // [B][F] node ids (unused at step 0)
@@ -157,15 +158,18 @@ struct DraftParams {
     int32_t* node_parent;             // [B][M]
     int32_t* node_token;
     float* node_score;
-    int32_t* tk_tok;                  // workspace: [B][F][k] per-row top-k
+    int32_t* tk_tok;                  // workspace: [B][F][S][k] top-k of each part of a row
     float* tk_lp;
     uint32_t* status;
     int B, F, V, k, step, M;
+    int S, chunk;                     // a row's vocabulary in S parts of `chunk` tokens (one CTA each)
 };
 struct RerankParams {
     const int32_t* node_parent;
     const int32_t* node_token;
     const float* node_score;
+    const int32_t* pool;              // [B][P] eligible node ids, or NULL: every node
+    int P;
     int32_t* parents;                 // [B][N]
     int32_t* tokens;
     uint32_t* status;

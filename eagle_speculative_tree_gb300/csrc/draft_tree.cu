@@ -1,6 +1,7 @@
 // Draft-tree construction: one beam-expansion step (tree_draft_step) and the final
-// rerank (tree_rerank).  Every scored candidate becomes a node; the k best of a step
-// form the next frontier; the rerank chooses among all nodes.
+// rerank (tree_rerank, tree_rerank_pool).  Every scored candidate becomes a node; the k
+// best of a step form the next frontier; the rerank chooses among all nodes or among a
+// given pool of them.
 //
 // Confidence of a draft path = product of its conditional probabilities ("EAGLE-2 &
 // Lookahead Decoding", section 4); in log space a node's score is its parent's score
@@ -25,20 +26,23 @@ __device__ __forceinline__ bool before(float av, int at, float bv, int bt) {
     return av > bv || (av == bv && at < bt);
 }
 
-// Top-k tokens of one frontier row.  Each warp keeps one sorted list spread over its
-// lanes (lane i holds rank i, i < k) and a copy of its k-th entry in every lane; the
-// lanes test their elements against that threshold with one ballot, and the rare
-// winners are inserted one at a time by shifting the list down a lane.  Then warp 0
-// ranks the warps' lists.  (With a private list per thread, some lane of a warp inserts
-// at almost every element and the warp runs the insertion nearly always.)
+// Top-k tokens of one part of a frontier row (a row's vocabulary is cut into p.S parts
+// of p.chunk tokens, one CTA each, so that the SMs share every row: one CTA per row left
+// most of them idle).  Each warp keeps one sorted list spread over its lanes (lane i
+// holds rank i, i < k) and a copy of its k-th entry in every lane; the lanes test their
+// elements against that threshold with one ballot, and the rare winners are inserted one
+// at a time by shifting the list down a lane.  Then warp 0 ranks the warps' lists.  (With
+// a private list per thread, some lane of a warp inserts at almost every element and the
+// warp runs the insertion nearly always.)
 template <bool VEC>
 __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftParams p) {
     constexpr int kWarps = kTopkThreads / 32;
     __shared__ float sv[kWarps * kMaxTopk];
     __shared__ int st[kWarps * kMaxTopk];
-    const int row = blockIdx.x;                           // b * F + f
+    const int row = blockIdx.x / p.S, part = blockIdx.x % p.S;   // row = b * F + f
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = p.k;
+    const int v_lo = part * p.chunk, v_hi = min(p.V, v_lo + p.chunk);
     const float* lp = p.logprobs + size_t(row) * p.V;
     float wv = -INFINITY, tv = -INFINITY;                // this lane's list entry; the warp's k-th entry
     int wt = INT_MAX, tt = INT_MAX;
@@ -70,19 +74,23 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
     // eight independent loads per lane in flight before they are consumed (four left a
     // CTA latency-bound at about 10 GB/s)
     constexpr int kU = 8;
-    if constexpr (VEC) {
-        for (int v0 = 0; v0 < p.V; v0 += kTopkThreads * 4 * kU) {
+    if constexpr (VEC) {                                  // p.chunk is a multiple of 4
+        for (int v0 = v_lo; v0 < v_hi; v0 += kTopkThreads * 4 * kU) {
             float4 x[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int v = v0 + (u * kTopkThreads + tid) * 4;
-                x[u] = v < p.V ? __ldg(reinterpret_cast<const float4*>(lp + v))
-                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                x[u] = v < v_hi ? __ldg(reinterpret_cast<const float4*>(lp + v))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
+                // one vote per float4: only a group holding a value at or above the warp's
+                // k-th entry can change the list (exact: a tie needs the token test below)
+                const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+                if (!__any_sync(0xffffffffu, m4 >= tv)) continue;
                 const int v = v0 + (u * kTopkThreads + tid) * 4;
-                const bool in = v < p.V;
+                const bool in = v < v_hi;
                 consider(x[u].x, in ? v : INT_MAX);
                 consider(x[u].y, in ? v + 1 : INT_MAX);
                 consider(x[u].z, in ? v + 2 : INT_MAX);
@@ -90,17 +98,17 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
             }
         }
     } else {
-        for (int v0 = 0; v0 < p.V; v0 += kTopkThreads * kU) {
+        for (int v0 = v_lo; v0 < v_hi; v0 += kTopkThreads * kU) {
             float x[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int v = v0 + u * kTopkThreads + tid;
-                x[u] = v < p.V ? __ldg(lp + v) : -INFINITY;
+                x[u] = v < v_hi ? __ldg(lp + v) : -INFINITY;
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int v = v0 + u * kTopkThreads + tid;
-                consider(x[u], v < p.V ? v : INT_MAX);
+                consider(x[u], v < v_hi ? v : INT_MAX);
             }
         }
     }
@@ -118,54 +126,74 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
                 const int oi = (o / k) * kMaxTopk + o % k;
                 rank += before(sv[oi], st[oi], sv[ci], st[ci]) ? 1 : 0;
             }
-            if (rank < k) {
-                p.tk_tok[size_t(row) * k + rank] = st[ci];
-                p.tk_lp[size_t(row) * k + rank] = sv[ci];
-                if (st[ci] == INT_MAX) atomicOr(p.status, TREESPEC_STATUS_BAD_TOKEN);   // fewer than k usable values
+            if (rank < k) {                               // a part shorter than k leaves INT_MAX entries
+                p.tk_tok[size_t(blockIdx.x) * k + rank] = st[ci];
+                p.tk_lp[size_t(blockIdx.x) * k + rank] = sv[ci];
             }
         }
     }
 }
 
-// One warp per sequence: write the F * k candidates as nodes base + (f * k + r), and the
-// k best (ties: lower candidate index) as the next frontier, best first.
-__global__ void __launch_bounds__(32) draft_select_kernel(const DraftParams p) {
+// One CTA per sequence.  First each frontier row's top k out of the S partial lists of
+// its parts (ties: lower token id); then the F * k candidates become nodes base + (f * k
+// + r), and the k best of them (ties: lower candidate index) the next frontier, best first.
+constexpr int kSelectThreads = 256;
+__global__ void __launch_bounds__(kSelectThreads) draft_select_kernel(const DraftParams p) {
     __shared__ float cs[kMaxFrontier * kMaxTopk];
-    const int b = blockIdx.x, lane = threadIdx.x;
-    const int k = p.k, F = p.F, nc = F * k;
+    __shared__ float mv[kMaxFrontier * kMaxTopk];
+    __shared__ int mt[kMaxFrontier * kMaxTopk];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int k = p.k, F = p.F, S = p.S, nc = F * k;
     int* par = p.node_parent + size_t(b) * p.M;
     int* tok = p.node_token + size_t(b) * p.M;
     float* sc = p.node_score + size_t(b) * p.M;
     const int base = p.step == 0 ? 1 : 1 + k + (p.step - 1) * k * k;
-    for (int c = lane; c < nc; c += 32) {
+    // merge: entry e = (f, part, r) of the F * S * k partial entries takes its rank within row f
+    const size_t e0 = size_t(b) * F * S * k;
+    for (int e = tid; e < F * S * k; e += kSelectThreads) {
+        const int f = e / (S * k);
+        const float ev = p.tk_lp[e0 + e];
+        const int et = p.tk_tok[e0 + e];
+        int rank = 0;
+        for (int o = f * S * k; o < (f + 1) * S * k; ++o) rank += before(p.tk_lp[e0 + o], p.tk_tok[e0 + o], ev, et) ? 1 : 0;
+        if (rank < k) {
+            mv[f * k + rank] = ev;
+            mt[f * k + rank] = et;
+            if (et == INT_MAX) atomicOr(p.status, TREESPEC_STATUS_BAD_TOKEN);   // fewer than k usable values
+        }
+    }
+    __syncthreads();
+    for (int c = tid; c < nc; c += kSelectThreads) {
         const int f = c / k;
         const int node = p.step == 0 ? 0 : p.frontier_in[size_t(b) * F + f];
         const float parent_score = p.step == 0 ? 0.f : sc[node];
-        const float score = parent_score + p.tk_lp[(size_t(b) * F + f) * k + c % k];
+        const float score = parent_score + mv[c];
         cs[c] = score;
         par[base + c] = node;
-        tok[base + c] = p.tk_tok[(size_t(b) * F + f) * k + c % k];
+        tok[base + c] = mt[c];
         sc[base + c] = score;
     }
-    __syncwarp();
-    for (int c = lane; c < nc; c += 32) {
+    __syncthreads();
+    for (int c = tid; c < nc; c += kSelectThreads) {
         int rank = 0;
         for (int o = 0; o < nc; ++o) rank += before(cs[o], o, cs[c], c) ? 1 : 0;
         if (rank < k) p.frontier_out[size_t(b) * k + rank] = base + c;
     }
-    if (p.step == 0 && lane == 0) {
+    if (p.step == 0 && tid == 0) {
         par[0] = -1;
         tok[0] = -1;
         sc[0] = 0.f;
     }
 }
 
-// One CTA per sequence: keep the root and the N - 1 best nodes, numbered by original
-// index, parents remapped.
+// One CTA per sequence: keep the root and the N - 1 best eligible nodes (every node, or
+// the pool's), numbered by original index, parents remapped; a pool with fewer eligible
+// nodes leaves the rest of the row as padding (parent kAbsent, token -1).
 __global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
     __shared__ float s[kMaxDraftNodes];
     __shared__ int par[kMaxDraftNodes];
     __shared__ int kept[kMaxDraftNodes], newidx[kMaxDraftNodes];
+    __shared__ unsigned char elig[kMaxDraftNodes];
     const int b = blockIdx.x, tid = threadIdx.x, M = p.M, N = p.N;
     for (int i = tid; i < M; i += blockDim.x) {
         s[i] = p.node_score[size_t(b) * M + i];
@@ -175,13 +203,21 @@ __global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
             q = 0;
         }
         par[i] = q;
+        elig[i] = p.pool == nullptr && i > 0;
     }
     __syncthreads();
+    if (p.pool) {                                         // ids outside 1 .. M-1 are ignored
+        for (int e = tid; e < p.P; e += blockDim.x) {
+            const int id = p.pool[size_t(b) * p.P + e];
+            if (id > 0 && id < M) elig[id] = 1;
+        }
+        __syncthreads();
+    }
     for (int i = tid; i < M; i += blockDim.x) {
         int rank = 0;
-        if (i > 0)
-            for (int j = 1; j < M; ++j) rank += before(s[j], j, s[i], i) ? 1 : 0;
-        kept[i] = i == 0 || rank < N - 1;
+        if (elig[i])
+            for (int j = 1; j < M; ++j) rank += (elig[j] && before(s[j], j, s[i], i)) ? 1 : 0;
+        kept[i] = i == 0 || (elig[i] && rank < N - 1);
     }
     __syncthreads();
     for (int i = tid; i < M; i += blockDim.x) {
@@ -190,6 +226,11 @@ __global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
         newidx[i] = n;                                    // root -> 0, kept nodes -> 1, 2, ...
     }
     __syncthreads();
+    const int nk = newidx[M - 1] + kept[M - 1];           // nodes kept, root included
+    for (int q = nk + tid; q < N; q += blockDim.x) {
+        p.parents[size_t(b) * N + q] = kAbsent;
+        p.tokens[size_t(b) * N + q] = -1;
+    }
     for (int i = tid; i < M; i += blockDim.x) {
         if (!kept[i]) continue;
         const int ni = newidx[i];
@@ -210,11 +251,11 @@ __global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
 }  // namespace
 
 cudaError_t launch_draft_step(const DraftParams& p, cudaStream_t s) {
-    const unsigned grid = unsigned(p.B) * unsigned(p.F);
+    const unsigned grid = unsigned(p.B) * unsigned(p.F) * unsigned(p.S);
     if (p.V % 4 == 0) draft_topk_kernel<true><<<grid, kTopkThreads, 0, s>>>(p);
     else draft_topk_kernel<false><<<grid, kTopkThreads, 0, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-    draft_select_kernel<<<unsigned(p.B), 32, 0, s>>>(p);
+    draft_select_kernel<<<unsigned(p.B), kSelectThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -344,6 +344,25 @@ int tree_rerank(const int32_t *node_parent, const int32_t *node_token, const flo
                 int32_t *tree_parents, int32_t *draft_tokens,
                 void *workspace, size_t workspace_bytes, treespec_stream_t stream);
 
+/*
+ * tree_rerank_pool -- tree_rerank among a given set of candidates.  The SGLang page's
+ * rerank may be read over all scored candidates (tree_rerank) or over the nodes that
+ * entered some step's beam (the reading under which 5 steps of top-4 rerank 20
+ * candidates): pass the union of the steps' frontier_out arrays as the pool.
+ *   pool [B][pool_size] int32: node ids eligible besides the root; ids outside
+ *        1 .. max_nodes-1 are ignored, duplicates count once.  1 <= pool_size <= 1024.
+ * Keeps the root and the num_nodes - 1 best pool nodes (ties: lower node index).  With
+ * fewer eligible nodes than num_nodes - 1 the tree is smaller: its row is padded after
+ * the last kept node with TREESPEC_ABSENT parents and token -1 (the padded layout the
+ * verify and accept calls take).  A kept node whose parent is not kept is attached to the
+ * root and sets TREESPEC_STATUS_BAD_PARENT.  Other arguments and limits as tree_rerank.
+ */
+int tree_rerank_pool(const int32_t *node_parent, const int32_t *node_token, const float *node_score,
+                     const int32_t *pool, int32_t pool_size,
+                     int32_t batch, int32_t max_nodes, int32_t num_nodes,
+                     int32_t *tree_parents, int32_t *draft_tokens,
+                     void *workspace, size_t workspace_bytes, treespec_stream_t stream);
+
 /* ------------------------------------------------------------------------- helpers */
 
 /* Synchronise `stream` and copy the status word of a workspace used by the last call

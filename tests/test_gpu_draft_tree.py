@@ -82,3 +82,60 @@ def test_rows_without_enough_values_are_flagged(ts, cuda_device):
     sc = torch.zeros((1, 5), dtype=torch.float32, device=cuda_device)
     _front, ws = ts.tree_draft_step(lp, 0, 2, None, par, tok, sc)
     assert ts.read_status(ws) & 8
+
+
+@pytest.mark.parametrize("name", ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy", "c3_llama2_7b_bf16_stoch",
+                                  "c4_llama3_70b_bf16_greedy", "c5_ragged_b64_bf16_stoch"])
+def test_entry_points_rebuild_the_generator_trees(ts, cuda_device, name):
+    """tree_draft_step x steps + the rerank, fed the generator's own child log-probabilities
+    (placed at random token ids of a 1000-token row, the rest far below), rebuild the
+    parent arrays gen.trees.build_tree makes for every workload: the rerank takes the
+    beam nodes (the union of the steps' frontiers) where the recipe's steps * topk >=
+    N - 1 -- c2's 20 candidates -- and every candidate otherwise."""
+    import gen
+    from gen import inputs as gi, trees
+    w = gen.get(name)
+    k, steps, N, V = w.topk, w.num_steps, w.num_nodes, 1000
+    M = odt.num_nodes_after(steps, k)
+    for b in range(min(w.batch, 4) if w.vary_tree else 1):
+        want = trees.build_tree(gi.rng_for(w, b, gi.TREE), steps, k, N)
+        rng = gi.rng_for(w, b, gi.TREE)
+        place = np.random.default_rng(1234 + b)
+        par = torch.zeros((1, M), dtype=torch.int32, device=cuda_device)
+        tok = torch.zeros_like(par)
+        sc = torch.zeros((1, M), dtype=torch.float32, device=cuda_device)
+        front, fronts = None, []
+        for s in range(steps):
+            F = 1 if s == 0 else k
+            rows = np.full((1, F, V), -1e30, np.float32)
+            for f in range(F):                       # draws in frontier order, as the generator expands
+                rows[0, f, place.choice(V, size=k, replace=False)] = trees._child_logprobs(rng, k).astype(np.float32)
+            front, ws = ts.tree_draft_step(torch.from_numpy(rows).to(cuda_device), s, k, front, par, tok, sc)
+            assert ts.read_status(ws) == 0
+            fronts.append(front)
+        pool = torch.cat(fronts, dim=1) if steps * k >= N - 1 else None
+        gp, _gt = ts.tree_rerank(par, tok, sc, N, pool=pool)
+        assert gp.cpu().numpy()[0].tolist() == want.tolist(), (name, b)
+
+
+@pytest.mark.parametrize("pool_size", [1, 5, 20, 200])
+def test_rerank_pool_matches_oracle(ts, cuda_device, pool_size):
+    """Random pools, with duplicates and ids out of range, some smaller than N - 1 (the tree
+    is then padded): GPU and oracle agree exactly."""
+    B, V, k, steps, N = 3, 5003, 4, 4, 16
+    M = odt.num_nodes_after(steps, k)
+    lps = [gd.draft_logprobs(900 + s, B, 1 if s == 0 else k, V) for s in range(steps)]
+    par = torch.zeros((B, M), dtype=torch.int32, device=cuda_device)
+    tok = torch.zeros_like(par)
+    sc = torch.zeros((B, M), dtype=torch.float32, device=cuda_device)
+    front = None
+    for s, lp in enumerate(lps):
+        front, _ws = ts.tree_draft_step(torch.from_numpy(lp).to(cuda_device), s, k, front, par, tok, sc)
+    rng = np.random.default_rng(pool_size)
+    pool = rng.integers(-3, M + 3, size=(B, pool_size)).astype(np.int32)
+    wsr = torch.empty(256, dtype=torch.uint8, device=cuda_device)
+    gp, gt = ts.tree_rerank(par, tok, sc, N, pool=torch.from_numpy(pool).to(cuda_device), workspace=wsr)
+    st = ts.read_status(wsr)
+    op, ot, ost = odt.rerank(par.cpu().numpy(), tok.cpu().numpy(), sc.cpu().numpy(), N, pool=pool)
+    assert np.array_equal(gp.cpu().numpy(), op) and np.array_equal(gt.cpu().numpy(), ot)
+    assert st == ost
