@@ -623,8 +623,7 @@ namespace cg = cooperative_groups;
 
 template <int CL>
 struct ClusterRed {
-    float f[2][CL];
-    double d[2][CL];
+    float f[2][CL], g[2][CL];
     int i[2][CL];
 };
 
@@ -634,21 +633,11 @@ struct ClusterRed {
 template <int NT, int CL>
 struct ClusterReducer {
     ClusterRed<CL>* cr;
-    double* redd;
     float* redf;
+    float* redg;
     int* redi;
     int phase = 0;
 
-    __device__ double sum(double v) {
-        cg::cluster_group cl = cg::this_cluster();
-        v = block_sum_d<NT>(v, redd);
-        if (threadIdx.x == 0) cr->d[phase][cl.block_rank()] = v;
-        cl.sync();
-        double t = 0.0;
-        for (int k = 0; k < CL; ++k) t += cl.map_shared_rank(cr, k)->d[phase][k];
-        phase ^= 1;
-        return t;
-    }
     // float sum (partials combined in rank order, so every CTA gets the same value)
     __device__ float sumf(float v) {
         cg::cluster_group cl = cg::this_cluster();
@@ -701,14 +690,14 @@ struct ClusterReducer {
         phase ^= 1;
         return gi == 0x7fffffff ? 0 : gi;
     }
-    // exclusive prefix (in rank order) of one double per CTA, and the total
-    __device__ double exclusive(double v, double* total) {
+    // exclusive prefix (in rank order) of one float per CTA, and the total
+    __device__ float exclusive(float v, float* total) {
         cg::cluster_group cl = cg::this_cluster();
-        if (threadIdx.x == 0) cr->d[phase][cl.block_rank()] = v;
+        if (threadIdx.x == 0) cr->f[phase][cl.block_rank()] = v;
         cl.sync();
-        double pre = 0.0, t = 0.0;
+        float pre = 0.f, t = 0.f;
         for (int k = 0; k < CL; ++k) {
-            const double x = cl.map_shared_rank(cr, k)->d[phase][k];
+            const float x = cl.map_shared_rank(cr, k)->f[phase][k];
             if (k < int(cl.block_rank())) pre += x;
             t += x;
         }
@@ -716,31 +705,61 @@ struct ClusterReducer {
         *total = t;
         return pre;
     }
+    // (max, sum) of softmax partials in one round: every thread brings an integer offset m
+    // at or above the max of its values (log2 units; -inf if it has none) and s = sum
+    // 2^(x - m); partials combine as M = max(m1, m2) and s1 2^(m1 - M) + s2 2^(m2 - M).  The
+    // offsets being integers, the rescales are exact powers of two and only the additions
+    // round, as in a plain sum.  Returns (M, S), the same everywhere.
+    __device__ float2 maxsum(float m, float s) {
+        cg::cluster_group cl = cg::this_cluster();
+        auto combine = [](float& m1, float& s1, float m2, float s2) {
+            const float M = fmaxf(m1, m2);
+            if (M == -INFINITY) return;                        // both empty
+            const float a = m1 == -INFINITY ? 0.f : ldexpf(s1, int(m1 - M));
+            const float c = m2 == -INFINITY ? 0.f : ldexpf(s2, int(m2 - M));
+            s1 = a + c;
+            m1 = M;
+        };
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            combine(m, s, m2, s2);
+        }
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        __syncthreads();
+        if (lane == 0) { redf[warp] = m; redg[warp] = s; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < NT / 32; ++w) combine(m, s, redf[w], redg[w]);
+            cr->f[phase][cl.block_rank()] = m;
+            cr->g[phase][cl.block_rank()] = s;
+        }
+        cl.sync();
+        float M = -INFINITY, S = 0.f;
+        for (int k = 0; k < CL; ++k) {                         // rank order: identical everywhere
+            const ClusterRed<CL>* r = cl.map_shared_rank(cr, k);
+            combine(M, S, r->f[phase][k], r->g[phase][k]);
+        }
+        phase ^= 1;
+        return make_float2(M, S);
+    }
 };
 
-template <int NT>
-__device__ __forceinline__ double block_exclusive_d(double v, double* scratch) {
-    // scratch: NT/32 + 1 doubles
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    double inc = warp_inclusive_scan_d(v);
-    __syncthreads();
-    if (lane == 31) scratch[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        const double x = lane < NT / 32 ? scratch[lane] : 0.0;
-        const double wi = warp_inclusive_scan_d(x);
-        if (lane < NT / 32) scratch[lane] = wi - x;           // exclusive per warp
+__device__ __forceinline__ float warp_inclusive_scan_f(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    __syncthreads();
-    return scratch[warp] + (inc - v);
+    return x;
 }
 
 template <int CL, int NT, int E, bool STOCH>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_cluster_kernel(AcceptParams p) {
     __shared__ int par[kMaxNodes], tok[kMaxNodes], path[kMaxNodes];
     __shared__ float izs[kMaxNodes], uni[kMaxNodes];
-    __shared__ double redd[32], scan[NT / 32 + 1];
-    __shared__ float redf[32];
+    __shared__ float redf[32], redg[32], scan[NT / 32 + 1];
     __shared__ int redi[32];
     __shared__ int s_cur, s_len, s_action, s_child, s_found;
     __shared__ float ch_lg[kMaxNodes], ch_q[kMaxNodes];     // target logit / draft prob of each child's token
@@ -755,7 +774,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     // warp-wide float4 load reads 512 contiguous bytes.
     const int wbase = (rank * (NT / 32) + warp) * 32 * E;
     auto tok_of = [&](int e) { return wbase + (e >> 2) * 128 + lane * 4 + (e & 3); };
-    ClusterReducer<NT, CL> red{&cred, redd, redf, redi, 0};
+    ClusterReducer<NT, CL> red{&cred, redf, redg, redi, 0};
 
     for (int c = tid; c < N; c += NT) {
         par[c] = p.parents[size_t(b) * N + c];
@@ -819,19 +838,24 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             }
             amax = red.argmax(best, bi);
         } else {
+            // max and sum in one cluster round: each thread's partial sum is taken against
+            // an integer offset at or above its own max, the reduction rescales the partials
+            // exactly, then p = 2^(x c - M2) / S is formed as prob_at forms it for the child
+            // tests (M2 the largest offset: at most one above the row's max)
             float m = -INFINITY;
 #pragma unroll
             for (int e = 0; e < E; ++e) m = fmaxf(m, r[e]);
-            M2 = red.max(m) * p.c;
+            const float mloc = m == -INFINITY ? -INFINITY : ceilf(m * p.c);   // c > 0 commutes with max
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            if (mloc != -INFINITY) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                r[e] = ex2(fmaf(r[e], p.c, -M2));                 // -inf (padding) -> 0
-                ls[e & 3] += r[e];
+                for (int e = 0; e < E; ++e) ls[e & 3] += ex2(fmaf(r[e], p.c, -mloc));
             }
-            invS = 1.f / red.sumf((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            const float2 ms = red.maxsum(mloc, (ls[0] + ls[1]) + (ls[2] + ls[3]));
+            M2 = ms.x;
+            invS = 1.f / ms.y;
 #pragma unroll
-            for (int e = 0; e < E; ++e) r[e] *= invS;               // r = p, as prob_at
+            for (int e = 0; e < E; ++e) r[e] = ex2(fmaf(r[e], p.c, -M2)) * invS;   // -inf (padding) -> 0
         }
         int jj = 0, pos = cur, action = 0, child = -1;
         for (;;) {
@@ -936,7 +960,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             return make_float4(fmaxf(r[e] - q4.x, 0.f), fmaxf(r[e + 1] - q4.y, 0.f), fmaxf(r[e + 2] - q4.z, 0.f),
                                fmaxf(r[e + 3] - q4.w, 0.f));
         };
-        double total = 0.0, wsum = 0.0;                      // wsum: this warp's weight
+        // Sums in float32 (GB300's float64 rate is a small fraction of its float32 rate):
+        // each thread's four running sums of at most 16 terms, then trees over the warp, the
+        // CTA and the cluster; the crossing warp walks its chunks with a compensated running
+        // sum.  Any prefix of the weights is then off by at most about (16 + 5 + 4 + 2 + 6)
+        // float32 roundings, 2e-6 of the total -- a tenth of the 2e-5 margin below which a
+        // decision counts as a rounding tie.
+        float total = 0.f, wsum = 0.f;                        // wsum: this warp's weight
         for (int attempt = 0; attempt < 2; ++attempt) {
             float m4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -947,31 +977,34 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                 m4[2] += w4.z;
                 m4[3] += w4.w;
             }
-            const double lane_sum = double((m4[0] + m4[1]) + (m4[2] + m4[3]));
-            wsum = __shfl_sync(0xffffffffu, warp_sum_d(lane_sum), 0);
-            total = red.sum(lane_sum);
-            if (total > 0.0 || rej == 0 || unchanged) break;
+            const float lane_sum = (m4[0] + m4[1]) + (m4[2] + m4[3]);
+            wsum = __shfl_sync(0xffffffffu, warp_sum(lane_sum), 0);
+            total = red.sumf(lane_sum);
+            if (total > 0.f || rej == 0 || unchanged) break;
             unchanged = true;                                // zero residual mass: keep r_{rej-1}
         }
-        // each warp's interval of the cumulative weight, in token order: warps of this CTA,
-        // then the CTAs of the cluster
+        // each warp's interval [base, end) of the cumulative weight, in token order: warps of
+        // this CTA, then the CTAs of the cluster.  A warp's end is the next warp's base, the
+        // same float expression, so the intervals tile the total without rounding gaps.
         if (lane == 0) scan[warp] = wsum;
         __syncthreads();
-        double pre_warp = 0.0, cta_total = 0.0;
+        float pre_warp = 0.f, pre_next = 0.f, cta_total = 0.f;
         for (int w2 = 0; w2 < NT / 32; ++w2) {
             if (w2 < warp) pre_warp += scan[w2];
+            if (w2 <= warp) pre_next += scan[w2];
             cta_total += scan[w2];
         }
-        double all = 0.0;
-        const double pre_cta = red.exclusive(cta_total, &all);
-        const double thr = double(uni[0]) * all;
-        const double base = pre_cta + pre_warp;
+        float all = 0.f;
+        const float pre_cta = red.exclusive(cta_total, &all);
+        const float thr = uni[0] * all;
+        const float base = pre_cta + pre_warp;
+        const float end = pre_cta + pre_next;
         if (tid == 0 && rank == 0) s_found = 0;
         cluster.sync();
-        if (base <= thr && thr < base + wsum) {              // warp-uniform: the crossing is in this warp
+        if (base <= thr && thr < end) {                      // warp-uniform: the crossing is in this warp
             // walk the warp's 128-token chunks in order; in the chunk that crosses, a scan
             // over the lanes' four tokens finds the lane, the lane finds the token
-            double run = base;
+            float run = base, comp = 0.f;                    // compensated running sum
             int v = -1, lnz = -1;
             bool done = false;
 #pragma unroll
@@ -982,24 +1015,26 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                 for (int u = 0; u < 4; ++u)
                     if (w[u] > 0.f) lnz = max(lnz, tok_of(e + u));
                 if (done) continue;
-                const double ls = ((double(w[0]) + double(w[1])) + double(w[2])) + double(w[3]);
-                const double incl = warp_inclusive_scan_d(ls);
-                const double ctot = __shfl_sync(0xffffffffu, incl, 31);
+                const float ls = ((w[0] + w[1]) + w[2]) + w[3];
+                const float incl = warp_inclusive_scan_f(ls);
+                const float ctot = __shfl_sync(0xffffffffu, incl, 31);
                 if (run + ctot > thr) {
                     const unsigned pass = __ballot_sync(0xffffffffu, run + incl > thr);
                     const int L = pass ? __ffs(pass) - 1 : 31;
                     if (lane == L) {
-                        double rr = run + (incl - ls);
+                        float rr = run + (incl - ls);
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            rr += double(w[u]);
+                            rr += w[u];
                             if (v < 0 && rr > thr) v = tok_of(e + u);
                         }
                     }
                     v = __shfl_sync(0xffffffffu, v, L);
                     done = true;
                 }
-                run += ctot;
+                const float y = ctot - comp, tsum = run + y;
+                comp = (tsum - run) - y;
+                run = tsum;
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lnz = max(lnz, __shfl_xor_sync(0xffffffffu, lnz, o));
@@ -1048,18 +1083,25 @@ template <bool STOCH>
 int launch_schedule(const AcceptParams& p, int mode, cudaStream_t s) {
     if (mode == TREESPEC_ACCEPT_PATH_ONLY) {
         const bool vec = p.V % 4 == 0 && p.B <= 65535;
-        // A row per cluster, 64 tokens per thread: clusters of 2 (76 fit on the GPU at
-        // once) up to 65,536 tokens, of 4 (36 at once) up to 131,072.
+        // A row per cluster, held in registers: clusters of 2 (76 fit on the GPU at once) up
+        // to 65,536 tokens, of 4 (36 at once) up to 131,072, with 32 or 64 tokens a thread.
+        // Where the batch leaves SMs idle the cluster doubles and each thread holds half as
+        // many tokens: the walk of a sequence is a chain of row loads and cluster-wide
+        // reductions, and both shorten with more SMs per row.
+        const bool wide = (long long)p.B * 8 <= p.sms;
         if (vec && p.V > 16384 && p.V <= 32768) {
-            accept_cluster_kernel<2, 512, 32, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
+            if (wide) accept_cluster_kernel<4, 512, 16, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
+            else accept_cluster_kernel<2, 512, 32, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
             return 1;
         }
         if (vec && p.V > 32768 && p.V <= 65536) {
-            accept_cluster_kernel<2, 512, 64, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
+            if (wide) accept_cluster_kernel<4, 512, 32, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
+            else accept_cluster_kernel<2, 512, 64, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
             return 1;
         }
         if (vec && p.V > 65536 && p.V <= 131072) {
-            accept_cluster_kernel<4, 512, 64, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
+            if (wide) accept_cluster_kernel<8, 512, 32, STOCH><<<dim3(8, p.B), 512, 0, s>>>(p);
+            else accept_cluster_kernel<4, 512, 64, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
             return 1;
         }
         if (p.V >= 32768) path_launch<512, STOCH>(p, s);

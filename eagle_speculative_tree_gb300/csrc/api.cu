@@ -338,6 +338,7 @@ extern "C" int tree_accept_with_mode(const float* target_logits, const int32_t* 
     p.V = vocab;
     p.temperature = temperature;
     p.c = stoch ? float(1.4426950408889634 / double(temperature)) : 0.f;
+    p.sms = sm_count_or_default();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     int kernels = 0;

@@ -118,6 +118,7 @@ struct AcceptParams {
     int B, N, V;
     float temperature;
     float c;          // log2(e) / temperature
+    int sms;          // SMs of the device (the cluster size of the walk depends on B / sms)
 };
 
 // Kernel launchers (each returns cudaGetLastError() of its launch).
