@@ -85,6 +85,26 @@ def attn_roofline(work, t_attn_ms, hbm, tf_burst):
                 kv_frac_cap=min(1.0, work["kv_bytes"] / max(t_tc, t_hbm) / 1e9 / hbm))
 
 
+def walk_row_bytes(path, alen, parents, vocab, greedy) -> int:
+    """Bytes of the rows an accept walk must read: each visited node's target row and, in a
+    stochastic walk, the draft row of each visited node at which a child was rejected."""
+    rows = 0
+    for b_ in range(len(alen)):
+        n = int(alen[b_])
+        nodes = [0] + [int(c) for c in path[b_, :n]]
+        par = parents[b_]
+        for i, cur in enumerate(nodes):
+            rows += 1
+            if greedy:
+                continue
+            kids = [k for k in range(len(par)) if par[k] == cur]
+            if i < n:
+                rows += kids[0] != nodes[i + 1]           # the accepted child is not the first
+            else:
+                rows += len(kids) > 0                     # every child was rejected
+    return rows * vocab * 4
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "eagle_speculative_tree_gb300", "csrc")
@@ -431,6 +451,44 @@ def run_gpu(args):
     row_bytes = w.vocab * 4 * (1 if w.greedy else 2)
     in_place = int((alen.to(torch.int64) + 1).sum().item()) * row_bytes
 
+    # ---- the accept walk alone with the rows in pinned host memory, against the link's
+    # copy rate: the rows it must fetch are the target row of every visited node and, where
+    # a child of that node was rejected, its draft row (each once)
+    for _ in range(3):
+        ts.tree_accept(rows_h["lg"], d["tok"], rows_h["qp"], d["par"], d["u"], w.temperature, accept_path=path,
+                       accept_len=alen, bonus_token=bonus, mode=args.accept_mode, workspace=ws_b, stream=stream)
+    torch.cuda.synchronize()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(K2):
+        ts.tree_accept(rows_h["lg"], d["tok"], rows_h["qp"], d["par"], d["u"], w.temperature, accept_path=path,
+                       accept_len=alen, bonus_token=bonus, mode=args.accept_mode, workspace=ws_b, stream=stream)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    ip_ms = a0.elapsed_time(a1) / K2
+    ip_bytes = walk_row_bytes(path.cpu().numpy(), alen.cpu().numpy(), x.tree_parents, w.vocab, w.greedy)
+    n_link = min(256 << 20, rows_h["lg"].numel() * 4)
+    src_link = rows_h["lg"].view(-1).view(torch.uint8)[:n_link]
+    dst_link = torch.empty(n_link, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        dst_link.copy_(src_link, non_blocking=True)
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(5):
+        dst_link.copy_(src_link, non_blocking=True)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    link_gbs = 5 * n_link / (l0.elapsed_time(l1) * 1e-3) / 1e9
+    del dst_link
+    ip_gbs = ip_bytes / (ip_ms * 1e-3) / 1e9
+    in_place_accept = {"ms": round(ip_ms, 4), "bytes": ip_bytes, "gbs": round(ip_gbs, 1),
+                       "link_copy_gbs": round(link_gbs, 1), "frac_of_link": round(ip_gbs / link_gbs, 3),
+                       "note": "tree_accept alone with target and draft rows in pinned host memory; bytes = the "
+                               "target row of each visited node + the draft row of each node with a rejected "
+                               "child, once each; link_copy_gbs = a 256 MiB pinned host-to-device copy"}
+
     # ---- KV commit of the accepted paths (not part of the step above): timed on the resident
     # pool with the accepted paths of the last step; it moves rows in place, so it runs last
     new_lens = torch.empty_like(d["pl"])
@@ -532,6 +590,7 @@ def run_gpu(args):
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "h2d_read_in_place_bytes_per_step_max": in_place,
+                "in_place_accept": in_place_accept,
                 "note": "q, page table, lengths, parents, tokens, uniforms copied in from pinned host memory and "
                         "attention output + accept results copied back, on a second stream overlapping the "
                         "neighbouring steps' compute; target logits and draft probabilities stay pinned on "

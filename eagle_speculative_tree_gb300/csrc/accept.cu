@@ -789,11 +789,21 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     uint32_t st = (tid == 0 && rank == 0) ? check_parents(par, N) : 0u;
 
     float r[E];
-    // the draft row is read only where a child is rejected (and for the bonus draw), from
-    // L1/L2, instead of being held in registers beside the target row
+    // The draft row is read only where a child is rejected (and for the bonus draw).  The
+    // first pass over it at a node stages this thread's E values in its own slots of shared
+    // memory ([E/4][NT] float4, conflict-free), and the later passes (the next siblings'
+    // residuals, the deferred rescale, the bonus draw) read them there: no other thread
+    // touches those slots, so no barrier is needed, and a row in host memory crosses the
+    // link once.
+    extern __shared__ float4 qstage[];
+    bool q_staged = false;                                  // the current node's row is staged
     auto q_at = [&](const float* q, int e) -> float4 {        // e a multiple of 4
+        float4* slot = qstage + (e >> 2) * NT + tid;
+        if (q_staged) return *slot;
         const int v = tok_of(e);
-        return v < V ? __ldg(reinterpret_cast<const float4*>(q + v)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x = v < V ? __ldg(reinterpret_cast<const float4*>(q + v)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        *slot = x;
+        return x;
     };
     const float* q_last = nullptr;                          // the draft row of the last visited node
     int amax = 0, rej = 0;
@@ -804,7 +814,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         const float* lg = p.logits + row * V;
         const float* qr = STOCH ? p.probs + row * V : nullptr;
         q_last = qr;
-        if (STOCH) {                                        // this warp's draft tokens, into L2 early
+        q_staged = false;
+        // this warp's draft tokens, into L2 early.  Not over the CPU-GPU link: there the
+        // link's rate bounds the walk, and the row is needed only if a child is rejected
+        // (the first child is accepted at about half of the levels).
+        if (STOCH && !p.probs_on_host) {
 #pragma unroll
             for (int m = 0; m < E / 32; ++m) {
                 const int v = wbase + (lane + 32 * m) * 32;    // one 128-byte line per lane
@@ -915,6 +929,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                     zs4[2] += fmaxf(r[e + 2] - q4.z, 0.f);
                     zs4[3] += fmaxf(r[e + 3] - q4.w, 0.f);
                 }
+                q_staged = true;
                 const float Z = red.sumf((zs4[0] + zs4[1]) + (zs4[2] + zs4[3]));
                 const float iz = Z > 0.f ? 1.f / Z : 0.f;
                 if (tid == 0) izs[jj - 1] = iz;
@@ -933,6 +948,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                     r[e + 2] = fmaxf(r[e + 2] - q4.z, 0.f) * piz;
                     r[e + 3] = fmaxf(r[e + 3] - q4.w, 0.f) * piz;
                 }
+                q_staged = true;
             }
             break;
         }
@@ -978,6 +994,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                 m4[3] += w4.w;
             }
             const float lane_sum = (m4[0] + m4[1]) + (m4[2] + m4[3]);
+            if (rej > 0 && !unchanged) q_staged = true;       // weight4 read every q slot
             wsum = __shfl_sync(0xffffffffu, warp_sum(lane_sum), 0);
             total = red.sumf(lane_sum);
             if (total > 0.f || rej == 0 || unchanged) break;
@@ -1079,6 +1096,16 @@ void path_launch(const AcceptParams& p, cudaStream_t s) {
     else accept_path_kernel<NT, false, STOCH><<<p.B, NT, 0, s>>>(p);
 }
 
+// The stochastic walk stages a draft row in NT * E floats of dynamic shared memory.
+template <int CL, int NT, int E, bool STOCH>
+void cluster_launch(const AcceptParams& p, cudaStream_t s) {
+    const int smem = STOCH ? NT * E * int(sizeof(float)) : 0;
+    if (STOCH)                                              // per call: the attribute is per device
+        cudaFuncSetAttribute(accept_cluster_kernel<CL, NT, E, STOCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    accept_cluster_kernel<CL, NT, E, STOCH><<<dim3(CL, p.B), NT, smem, s>>>(p);
+}
+
 template <bool STOCH>
 int launch_schedule(const AcceptParams& p, int mode, cudaStream_t s) {
     if (mode == TREESPEC_ACCEPT_PATH_ONLY) {
@@ -1090,18 +1117,18 @@ int launch_schedule(const AcceptParams& p, int mode, cudaStream_t s) {
         // reductions, and both shorten with more SMs per row.
         const bool wide = (long long)p.B * 8 <= p.sms;
         if (vec && p.V > 16384 && p.V <= 32768) {
-            if (wide) accept_cluster_kernel<4, 512, 16, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
-            else accept_cluster_kernel<2, 512, 32, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
+            if (wide) cluster_launch<4, 512, 16, STOCH>(p, s);
+            else cluster_launch<2, 512, 32, STOCH>(p, s);
             return 1;
         }
         if (vec && p.V > 32768 && p.V <= 65536) {
-            if (wide) accept_cluster_kernel<4, 512, 32, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
-            else accept_cluster_kernel<2, 512, 64, STOCH><<<dim3(2, p.B), 512, 0, s>>>(p);
+            if (wide) cluster_launch<4, 512, 32, STOCH>(p, s);
+            else cluster_launch<2, 512, 64, STOCH>(p, s);
             return 1;
         }
         if (vec && p.V > 65536 && p.V <= 131072) {
-            if (wide) accept_cluster_kernel<8, 512, 32, STOCH><<<dim3(8, p.B), 512, 0, s>>>(p);
-            else accept_cluster_kernel<4, 512, 64, STOCH><<<dim3(4, p.B), 512, 0, s>>>(p);
+            if (wide) cluster_launch<8, 512, 32, STOCH>(p, s);
+            else cluster_launch<4, 512, 64, STOCH>(p, s);
             return 1;
         }
         if (p.V >= 32768) path_launch<512, STOCH>(p, s);

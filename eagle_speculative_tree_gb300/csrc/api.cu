@@ -339,6 +339,11 @@ extern "C" int tree_accept_with_mode(const float* target_logits, const int32_t* 
     p.temperature = temperature;
     p.c = stoch ? float(1.4426950408889634 / double(temperature)) : 0.f;
     p.sms = sm_count_or_default();
+    if (stoch) {
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, draft_probs) == cudaSuccess) p.probs_on_host = at.type == cudaMemoryTypeHost;
+        else cudaGetLastError();                         // not a pointer CUDA knows: treat as device memory
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     int kernels = 0;

@@ -119,6 +119,8 @@ struct AcceptParams {
     float temperature;
     float c;          // log2(e) / temperature
     int sms;          // SMs of the device (the cluster size of the walk depends on B / sms)
+    int probs_on_host;  // draft_probs is host memory read over the CPU-GPU link: fetch a draft
+                        // row only where a child is rejected, never ahead
 };
 
 // Kernel launchers (each returns cudaGetLastError() of its launch).
