@@ -66,7 +66,8 @@ SWEEP = ["c1_tiny_f32_greedy", "c2_llama3_8b_bf16_greedy", "c3_llama2_7b_bf16_st
          "c4_llama3_70b_bf16_greedy@b1", "c4_llama3_70b_bf16_t0.7@b1",
          "c4_llama3_70b_bf16_greedy@b8", "c4_llama3_70b_bf16_t0.7@b8",
          "c4_llama3_70b_bf16_greedy", "c4_llama3_70b_bf16_t0.7", "c5_ragged_b64_bf16_stoch"]
-KERNEL_NAMES = {1: "attn_simt_kernel", 2: "attn_tc_kernel<false>", 3: "attn_tc_pair_kernel", 4: "attn_tc_kernel<true>"}
+KERNEL_NAMES = {1: "attn_simt_kernel", 2: "attn_tc_kernel<false>", 3: "attn_tc_pair_kernel<false>",
+                4: "attn_tc_kernel<true>", 5: "attn_tc_pair_kernel<true>"}
 L2_FLUSH_BYTES = 512 << 20       # written before every timed call of the sweep: 4x the 129 MB L2
 
 

@@ -25,7 +25,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 DTYPE_F32, DTYPE_BF16 = 0, 1
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC_PAIR, KERNEL_TC_2SM = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC_PAIR, KERNEL_TC_2SM, KERNEL_TC_STREAM = 0, 1, 2, 3, 4, 5
 ACCEPT_AUTO, ACCEPT_ALL_ROWS, ACCEPT_PATH_ONLY = 0, 1, 2
 ABSENT = -2                     # parent entry of a padding slot after a smaller tree
 STATUS_BITS = {1: "BAD_PARENT", 2: "BAD_PAGE", 4: "BAD_LENGTH", 8: "BAD_TOKEN", 16: "TIMEOUT", 32: "INTERNAL",

@@ -59,6 +59,16 @@ int sm_count_or_default() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The persistent two-tile kernel keeps the batch's 64-token tile offsets in shared memory
+// and its tile positions (over row-block pairs, sequences and kv heads) as int32: at most
+// kStreamMaxBatch sequences and fewer than 2^31 positions.
+bool stream_fits(const treespec_attn_shape& s) {
+    const long long tiles = ((long long)s.max_pages_per_seq * s.page_size + 63) / 64 + 3;   // + tree nodes
+    const long long G = s.num_q_heads / s.num_kv_heads;
+    const long long pairs = ((long long)s.num_nodes * G + 255) / 256;
+    return s.batch <= kStreamMaxBatch && pairs * s.num_kv_heads * s.batch * tiles < (1ll << 31);
+}
+
 int check_attn_shape(const treespec_attn_shape* s) {
     if (!s) return TREESPEC_ERR_NULL_POINTER;
     if (s->dtype != TREESPEC_DTYPE_F32 && s->dtype != TREESPEC_DTYPE_BF16) return TREESPEC_ERR_DTYPE;
@@ -71,14 +81,14 @@ int check_attn_shape(const treespec_attn_shape* s) {
     if ((long long)s->max_pages_per_seq * s->page_size > (1ll << 30)) return TREESPEC_ERR_SHAPE;
     const long long R = (long long)s->num_nodes * (s->num_q_heads / s->num_kv_heads);
     if (R > 4096 || (long long)s->num_kv_heads * ((R + 63) / 64) > 65535) return TREESPEC_ERR_SHAPE;
-    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC_2SM) return TREESPEC_ERR_SHAPE;
+    if (s->kernel < TREESPEC_KERNEL_AUTO || s->kernel > TREESPEC_KERNEL_TC_STREAM) return TREESPEC_ERR_SHAPE;
     if (s->num_splits < 0) return TREESPEC_ERR_SHAPE;
-    if (s->kernel == TREESPEC_KERNEL_TC || s->kernel == TREESPEC_KERNEL_TC_PAIR || s->kernel == TREESPEC_KERNEL_TC_2SM) {
+    if (s->kernel >= TREESPEC_KERNEL_TC) {
         if (!attn_tc_supported(s->dtype, s->head_dim)) return TREESPEC_ERR_DTYPE;
         if ((long long)s->num_pool_pages * s->page_size >= (1ll << 31)) return TREESPEC_ERR_SHAPE;
     }
-    if ((s->kernel == TREESPEC_KERNEL_TC_PAIR || s->kernel == TREESPEC_KERNEL_TC_2SM) && ((R + 127) / 128) % 2 != 0)
-        return TREESPEC_ERR_SHAPE;
+    if (s->kernel >= TREESPEC_KERNEL_TC_PAIR && ((R + 127) / 128) % 2 != 0) return TREESPEC_ERR_SHAPE;
+    if (s->kernel == TREESPEC_KERNEL_TC_STREAM && !stream_fits(*s)) return TREESPEC_ERR_SHAPE;
     return TREESPEC_OK;
 }
 
@@ -97,17 +107,20 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     // Measured at 64 q / 8 kv heads, 64 nodes, 8192-token prefixes (ms, CTA pair / two-tile /
     // one-tile): batch 2 0.080 / 0.088 / -, batch 8 0.149 / 0.169 / 0.169, batch 16
     // 0.279 / 0.243 / 0.315, batch 32 0.491 / 0.474 / 0.543.
-    if (s.kernel == TREESPEC_KERNEL_TC || s.kernel == TREESPEC_KERNEL_TC_PAIR || s.kernel == TREESPEC_KERNEL_TC_2SM ||
-        (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
+    if (s.kernel >= TREESPEC_KERNEL_TC || (s.kernel == TREESPEC_KERNEL_AUTO && tc_ok)) {
         const long long rbs = (R + 127) / 128;
         const bool paired = rbs % 2 == 0;
-        const bool small = (long long)s.batch * s.num_kv_heads * (rbs / 2) < sms;
-        p.kernel = s.kernel == TREESPEC_KERNEL_TC       ? TREESPEC_KERNEL_TC
-                   : s.kernel == TREESPEC_KERNEL_TC_2SM ? TREESPEC_KERNEL_TC_2SM
-                   : s.kernel == TREESPEC_KERNEL_TC_PAIR ? TREESPEC_KERNEL_TC_PAIR
-                   : !paired                             ? TREESPEC_KERNEL_TC
-                   : small                               ? TREESPEC_KERNEL_TC_2SM
-                                                         : TREESPEC_KERNEL_TC_PAIR;
+        const long long pair_units = (long long)s.batch * s.num_kv_heads * (rbs / 2);
+        const bool small = pair_units < sms;
+        // the persistent form pays a merge of the cut units and a few us per unit change,
+        // which two waves of two-tile CTAs or more amortise (measured: batch 32 0.460 ms
+        // against 0.473, batch 16 0.255 against 0.250)
+        const bool many = pair_units >= 2ll * sms;
+        p.kernel = s.kernel != TREESPEC_KERNEL_AUTO ? s.kernel
+                   : !paired                        ? TREESPEC_KERNEL_TC
+                   : small                          ? TREESPEC_KERNEL_TC_2SM
+                   : (many && stream_fits(s))       ? TREESPEC_KERNEL_TC_STREAM
+                                                    : TREESPEC_KERNEL_TC_PAIR;
         p.rows_per_block = 128;
     } else {
         p.kernel = TREESPEC_KERNEL_SIMT;
@@ -152,6 +165,12 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
         p.split_tokens = (p.split_tokens + tile - 1) / tile * tile;
     }
     p.merge = p.num_splits > 1;
+    if (p.kernel == TREESPEC_KERNEL_TC_STREAM) {   // no splits: the SMs share the tiles evenly
+        p.num_splits = 1;
+        p.split_tokens = int(std::min<long long>(max_tokens + 128, 1ll << 30));
+        p.merge = 0;
+        p.stream_ctas = std::min(sms, kStreamMaxCtas);
+    }
     return p;
 }
 
@@ -172,6 +191,17 @@ AttnLayout attn_layout(const treespec_attn_shape& s, const AttnPlan& p) {
     off = align_up(off + parts * 2 * 4, kWsAlign);
     L.acc = off;
     off = align_up(off + parts * s.head_dim * 4, kWsAlign);
+    if (p.kernel == TREESPEC_KERNEL_TC_STREAM) {
+        // two partial slots of 2 x 128 rows per CTA for the pieces of cut units, and their
+        // ready flags
+        const size_t rows = size_t(2) * p.stream_ctas * 256;
+        L.ml = off;
+        off = align_up(off + rows * 2 * 4, kWsAlign);
+        L.acc = off;
+        off = align_up(off + rows * s.head_dim * 4, kWsAlign);
+        L.flags = off;
+        off = align_up(off + size_t(2) * p.stream_ctas * 2 * 4, kWsAlign);
+    }
     L.total = off;
     return L;
 }
@@ -273,12 +303,15 @@ extern "C" int tree_attn_verify(const void* q, const void* k_pages, const void* 
     p.merge = plan.merge;
     p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(s.head_dim)));
     p.wait_ns = g_wait_ns.load();
+    p.stream_ctas = plan.stream_ctas;
+    p.stream_flags = plan.kernel == TREESPEC_KERNEL_TC_STREAM ? reinterpret_cast<int32_t*>(ws + lay.flags) : nullptr;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     if (launch_tree_prologue(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches++;
-    const cudaError_t e = plan.kernel == TREESPEC_KERNEL_TC_PAIR ? launch_attn_tc_pair(p, st)
+    const cudaError_t e = plan.kernel == TREESPEC_KERNEL_TC_STREAM ? launch_attn_tc_stream(p, st)
+                          : plan.kernel == TREESPEC_KERNEL_TC_PAIR ? launch_attn_tc_pair(p, st)
                           : plan.kernel == TREESPEC_KERNEL_TC_2SM ? launch_attn_tc_2sm(p, st)
                           : plan.kernel == TREESPEC_KERNEL_TC    ? launch_attn_tc(p, st)
                                                                  : launch_attn_simt(p, s.dtype, st);

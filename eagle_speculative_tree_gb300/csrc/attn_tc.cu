@@ -206,7 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.npg = (kPair && !is_v) ? 4 : 8;
         a.dp0 = (kPair && is_v) ? int(rank) : 0;
         a.ndp = (kPair && is_v) ? 1 : 2;
-        tcparts::produce_pages<kBN>(p, a, b, h, t0, t1, L, ntiles, abort_flag);
+        int armed = 0;
+        tcparts::produce_pages<kBN>(p, a, b, h, t0, t1, L, ntiles, armed, abort_flag);
+        tcparts::drain_copies(a, armed);
     } else if (warp == 1 && kPair && rank == 1) {
         // ------------------------------------------------------------ stage forwarder (pair, rank 1)
         // Rank 0's MMAs read this CTA's half of each stage: tell rank 0 when it has landed,

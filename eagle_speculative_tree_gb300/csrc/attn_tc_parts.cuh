@@ -27,8 +27,10 @@ constexpr int kBN = 128;     // tokens per KV tile of the one-tile and CTA-pair 
 // full page in the pool arrives by TMA (one copy per panel, 2048 bytes), the partly filled
 // last page of the sequence, a bad page id (flagged, then zero-filled) and pages past the
 // split are written by the warp itself.  A stage is rearmed once `empty` has completed for
-// its previous use.  On a timeout or an abort of the CTA the warp stops, then waits (under
-// the default bound) for the copies it has started before it returns.
+// its previous use.  `g` counts the tiles this warp has armed over the CTA's life (stage
+// g % nst, its (g / nst)-th use): a CTA that streams several ranges calls this once per
+// range and then drain_copies once.  On a timeout or an abort of the CTA the warp stops
+// and returns false.
 struct ProducerArgs {
     const CUtensorMap* map;
     const uint16_t* src;          // the pool [P][16][Hkv][128] (bf16 bits)
@@ -40,8 +42,8 @@ struct ProducerArgs {
 };
 
 template <int TILE>
-__device__ __forceinline__ void produce_pages(const AttnParams& p, const ProducerArgs& a, int b, int h, int t0,
-                                              int t1, int L, int ntiles, volatile uint32_t* abort_flag) {
+__device__ __forceinline__ bool produce_pages(const AttnParams& p, const ProducerArgs& a, int b, int h, int t0,
+                                              int t1, int L, int ntiles, int& g, volatile uint32_t* abort_flag) {
     constexpr int kPPT = TILE / 16;                    // pages per tile
     constexpr int kTPB = 32 / kPPT;                    // tiles per warp-wide page-id load
     const int lane = threadIdx.x & 31;
@@ -56,9 +58,8 @@ __device__ __forceinline__ void produce_pages(const AttnParams& p, const Produce
         return (jt < ntiles && pos0 < t1) ? __ldg(ptab + (pos0 >> 4)) : -1;
     };
     int batch_cur = fetch_batch(0), batch_next = fetch_batch(1);
-    int armed = 0;                                      // tiles whose stage this warp armed
-    for (int j = 0; j < ntiles; ++j) {
-        const int stage = j % a.nst;
+    for (int j = 0; j < ntiles; ++j, ++g) {
+        const int stage = g % a.nst;
         if (j > 0 && (j % kTPB) == 0) {
             batch_cur = batch_next;
             batch_next = fetch_batch(j / kTPB + 1);
@@ -79,11 +80,11 @@ __device__ __forceinline__ void produce_pages(const AttnParams& p, const Produce
                 page = -1;
             }
         }
-        if (j >= a.nst && !mbar_wait_bounded(&a.empty[stage], ((j / a.nst) - 1) & 1, p.wait_ns)) {
+        if (g >= a.nst && !mbar_wait_bounded(&a.empty[stage], ((g / a.nst) - 1) & 1, p.wait_ns)) {
             *abort_flag = 1;
             atomicOr(p.status, TREESPEC_STATUS_TIMEOUT);
         }
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
         unsigned char* dst = a.ring + stage * a.stage_bytes;
         const unsigned manual = __ballot_sync(0xffffffffu, kind == 2);
         if (manual) {
@@ -115,11 +116,15 @@ __device__ __forceinline__ void produce_pages(const AttnParams& p, const Produce
                 tma_load_3d(dst + dp * a.panel_bytes + lane * 2048, a.map, 64 * (a.dp0 + dp), h, z, &a.full[stage]);
         }
         __syncwarp();
-        ++armed;
     }
-    // Every copy this warp started has landed before the CTA may end: after an abort the
-    // consumers no longer wait for them.  The last phase armed on each stage completes
-    // once its copies arrive (earlier phases completed before it was armed).
+    return true;
+}
+
+// Every copy the warp started (`armed` tiles over the CTA's life) has landed before the
+// CTA may end: after an abort the consumers no longer wait for them.  The last phase armed
+// on each stage completes once its copies arrive (earlier phases completed before it was
+// armed).
+__device__ __forceinline__ void drain_copies(const ProducerArgs& a, int armed) {
     for (int s2 = 0; s2 < a.nst && s2 < armed; ++s2) {
         const int last = s2 + ((armed - 1 - s2) / a.nst) * a.nst;
         mbar_wait_bounded(&a.full[s2], uint32_t(last / a.nst) & 1u, kDefaultWaitNs);

@@ -13,6 +13,8 @@ namespace treespec {
 // (word w holds nodes 64w .. 64w+63): one word covers the 64-node trees of the radar
 // page's single-word mask, two cover trees of up to 128 nodes.
 constexpr int kMaxNodes = 128;
+constexpr int kStreamMaxBatch = 256;   // persistent two-tile attention: sequences per call
+constexpr int kStreamMaxCtas = 1024;   // persistent two-tile attention: CTAs (one per SM)
 constexpr int kAncWords = 2;
 constexpr int kAbsent = TREESPEC_ABSENT;   // parent entry of a padding slot past the end of a smaller tree
 constexpr size_t kWsAlign = 256;
@@ -64,16 +66,17 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 
 // Workspace of tree_attn_verify (offsets in bytes from the workspace base).
 struct AttnLayout {
-    size_t status, anc, lens, nn, ml, acc, total;
+    size_t status, anc, lens, nn, ml, acc, flags, total;
 };
 
 struct AttnPlan {
-    int kernel;          // TREESPEC_KERNEL_SIMT / _TC / _TC_PAIR / _TC_2SM
+    int kernel;          // TREESPEC_KERNEL_SIMT / _TC / _TC_PAIR / _TC_2SM / _TC_STREAM
     int num_splits;
     int split_tokens;
     int rows_per_block;
     int row_blocks;
     int merge;
+    int stream_ctas;     // _TC_STREAM: persistent CTAs (one per SM)
 };
 
 struct AttnParams {
@@ -93,6 +96,9 @@ struct AttnParams {
     int B, N, Hq, Hkv, G, R, D, ps, max_pages, num_pool_pages;
     int num_splits, split_tokens, rows_per_block, row_blocks, merge;
     float scale_log2;             // log2(e) / sqrt(D)
+    int stream_ctas;              // persistent two-tile kernel: CTAs (one per SM)
+    int32_t* stream_flags;        // persistent two-tile kernel: [2 * CTAs][2] a piece's partial is written
+                                  // (slot, query tile); zeroed by the prologue
     uint64_t wait_ns;             // bound of the tensor-core kernels' pipeline waits (kDefaultWaitNs unless a test shortens it)
 };
 
@@ -129,6 +135,7 @@ cudaError_t launch_attn_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_tc_2sm(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_tc_pair(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_tc_stream(const AttnParams& p, cudaStream_t s);
 bool attn_tc_supported(int dtype, int D);
 // TMA map of a K or V page pool [P][16][Hkv][128] bf16, one page x 64 head dims per box
 bool make_pool_map(CUtensorMap* map, const void* base, int Hkv, long long pool_tokens);

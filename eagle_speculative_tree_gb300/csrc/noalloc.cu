@@ -64,11 +64,17 @@ extern "C" int tree_attn_verify_noalloc(const void* q, const void* k_pages, cons
     treespec_attn_plan plan;
     const int rc = treespec_attn_plan_for(shape, &plan);
     if (rc != TREESPEC_OK) return rc;
-    if (treespec_attn_workspace_bytes(shape) > kScratchBytes) return TREESPEC_ERR_WORKSPACE;
+    treespec_attn_shape sh = *shape;
+    // The persistent two-tile kernel's partial slots (about 40 MB on 152 SMs) do not fit the
+    // array: an automatic plan that picks it runs the two-tile kernel one range per CTA.
+    if (sh.kernel == TREESPEC_KERNEL_AUTO && plan.kernel == TREESPEC_KERNEL_TC_STREAM &&
+        treespec_attn_workspace_bytes(&sh) > kScratchBytes)
+        sh.kernel = TREESPEC_KERNEL_TC_PAIR;
+    if (treespec_attn_workspace_bytes(&sh) > kScratchBytes) return TREESPEC_ERR_WORKSPACE;
     void* scratch = nullptr;
     const int dev_rc = scratch_of_current_device(&scratch);
     if (dev_rc != TREESPEC_OK) return dev_rc;
-    return tree_attn_verify(q, k_pages, v_pages, page_table, prefix_lens, tree_parents, out, shape, scratch,
+    return tree_attn_verify(q, k_pages, v_pages, page_table, prefix_lens, tree_parents, out, &sh, scratch,
                             kScratchBytes, stream);
 }
 

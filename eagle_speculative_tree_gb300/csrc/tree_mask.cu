@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kMaxNodes) tree_prologue_kernel(AttnParams p) 
         p.anc[((size_t)b * N + i) * kAncWords] = w0;
         p.anc[((size_t)b * N + i) * kAncWords + 1] = w1;
     }
+    if (p.stream_flags && b == 0)         // the persistent kernel's piece flags
+        for (int e = i; e < 2 * p.stream_ctas * 2; e += kMaxNodes) p.stream_flags[e] = 0;
     if (i == 0) {
         p.nn[b] = nb;
         int S = p.prefix_lens[b];

@@ -67,6 +67,10 @@ enum treespec_kernel {
     TREESPEC_KERNEL_TC_2SM = 4,   /* tcgen05/TMA split-KV kernel whose MMAs span a pair of CTAs (cta_group::2):
                                      two 128-row blocks per cluster of two SMs, each SM copying half of every K/V
                                      tile (bf16, head_dim 128, an even number of 128-row blocks) */
+    TREESPEC_KERNEL_TC_STREAM = 5,  /* the two-tile kernel as one persistent CTA per SM: every SM takes an equal
+                                       share of all KV tiles, a kv head's range cut between SMs is merged by the
+                                       SM that finishes it last (bf16, head_dim 128, an even number of 128-row
+                                       blocks, batch <= 256); num_splits does not apply */
 };
 
 enum treespec_accept_mode {

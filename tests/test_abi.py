@@ -84,8 +84,15 @@ def test_plan_pairs_query_tiles_when_the_row_blocks_pair_up():
     wide = dict(num_nodes=64, num_q_heads=64, num_kv_heads=8)      # 512 rows: four 128-row blocks
     b8 = ts.attn_plan(shape(batch=8, **wide))                      # 128 two-tile CTAs: under one wave
     assert b8.kernel == ts.KERNEL_TC_2SM and b8.rows_per_block == 128 and b8.row_blocks == 4
-    assert ts.attn_plan(shape(batch=32, **wide)).kernel == ts.KERNEL_TC_PAIR    # 512 two-tile CTAs
-    assert ts.attn_plan(shape(batch=10, **wide)).kernel == ts.KERNEL_TC_PAIR    # 160 two-tile CTAs: a wave and more
+    # two waves of two-tile CTAs or more: the persistent form, one CTA per SM
+    b32 = ts.attn_plan(shape(batch=32, **wide))
+    assert b32.kernel == ts.KERNEL_TC_STREAM and b32.num_splits == 1 and b32.merge == 0
+    assert ts.attn_plan(shape(batch=19, **wide)).kernel == ts.KERNEL_TC_STREAM  # 304 two-tile units
+    assert ts.attn_plan(shape(batch=18, **wide)).kernel == ts.KERNEL_TC_PAIR    # 288: under two waves
+    assert ts.attn_plan(shape(batch=10, **wide)).kernel == ts.KERNEL_TC_PAIR    # 160: a wave and more
+    assert ts.attn_plan(shape(batch=257, **wide)).kernel == ts.KERNEL_TC_PAIR   # past its batch limit
+    with pytest.raises(ValueError):                                                # refused, not truncated
+        ts.attn_workspace_bytes(shape(batch=257, kernel=ts.KERNEL_TC_STREAM, **wide))
     assert ts.attn_plan(shape(batch=9, **wide)).kernel == ts.KERNEL_TC_2SM      # 144: under one wave
     assert ts.attn_plan(shape(batch=1, **wide)).kernel == ts.KERNEL_TC_2SM
     assert ts.attn_plan(shape(batch=8, kernel=ts.KERNEL_TC, **wide)).kernel == ts.KERNEL_TC

@@ -41,7 +41,7 @@ def row_blocks(w):
     return -(-w.num_nodes * w.group // 128)
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5])
 @pytest.mark.parametrize("name,batch", SMALL)
 def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
     w = gen.get(name)
@@ -49,7 +49,7 @@ def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
         w = w.with_batch(batch)
     if kernel >= 2 and w.dtype != "bf16":
         pytest.skip("the tensor-core kernels take bf16")
-    if kernel in (3, 4) and row_blocks(w) % 2:
+    if kernel >= 3 and row_blocks(w) % 2:
         pytest.skip("the two-tile and CTA-pair kernels need an even number of 128-row blocks")
     x = gi.make_inputs(w, with_accept=False)
     out = run(ts, x, cuda_device, kernel=kernel)
@@ -58,7 +58,7 @@ def test_configs_match_oracle(ts, cuda_device, name, batch, kernel):
 
 def test_auto_plan_picks_tensor_cores_for_bf16_head128(ts, cuda_device):
     for name, want in [("c2_llama3_8b_bf16_greedy", 2), ("c3_llama2_7b_bf16_stoch", 2),
-                       ("c4_llama3_70b_bf16_greedy", 3), ("c5_ragged_b64_bf16_stoch", 2),
+                       ("c4_llama3_70b_bf16_greedy", 5), ("c5_ragged_b64_bf16_stoch", 2),
                        ("c1_tiny_f32_greedy", 1)]:
         w = gen.get(name)
         prob = ts.AttnProblem(w.batch, w.num_nodes, w.num_q_heads, w.num_kv_heads, w.head_dim, 16, 64, 100,
@@ -87,7 +87,8 @@ def _custom(name, parents, prefix, batch=None):
 
 @pytest.mark.parametrize("dtype_cfg,kernel", [("c1_tiny_f32_greedy", 1), ("c2_llama3_8b_bf16_greedy", 1),
                                               ("c2_llama3_8b_bf16_greedy", 2), ("c4_llama3_70b_bf16_greedy", 2),
-                                              ("c4_llama3_70b_bf16_greedy", 3), ("c4_llama3_70b_bf16_greedy", 4)])
+                                              ("c4_llama3_70b_bf16_greedy", 3), ("c4_llama3_70b_bf16_greedy", 4),
+                                              ("c4_llama3_70b_bf16_greedy", 5)])
 @pytest.mark.parametrize("case", ["single_node", "prefix0", "ragged_tail", "chain64", "star64",
                                   "random64", "random32", "chain128", "star128", "random128", "random100"])
 def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
@@ -115,7 +116,7 @@ def test_edge_cases(ts, cuda_device, dtype_cfg, kernel, case):
     else:
         parents, prefix = [trees.random_recursive(rng, 64), trees.random_recursive(rng, 64)], [5, 999]
     w, x = _custom(dtype_cfg, parents, prefix)
-    if kernel in (3, 4) and row_blocks(w) % 2:
+    if kernel >= 3 and row_blocks(w) % 2:
         pytest.skip("the two-tile and CTA-pair kernels need an even number of 128-row blocks")
     out = run(ts, x, cuda_device, kernel=kernel)
     assert_attention_close(out, oracle_attention(x), w.dtype)
@@ -174,7 +175,7 @@ def test_full_size_bench_workload_sampled(ts, cuda_device):
     w = gen.get(name)
     x = gi.make_inputs(w, with_accept=False)
     d = attn_device_inputs(x, cuda_device)
-    assert ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])).kernel == ts.KERNEL_TC_PAIR
+    assert ts.attn_plan(ts.attn_problem(d["q"], d["k_pages"], d["page_table"])).kernel == ts.KERNEL_TC_STREAM
     out = run(ts, x, cuda_device)
     pairs = full_size_pairs(w, 16, 0)
     ref = oracle_attention_pairs(name, pairs, workers=8)
@@ -229,7 +230,7 @@ def test_two_tile_kernel_refuses_an_odd_number_of_row_blocks(ts, cuda_device):
         run(ts, x, cuda_device, kernel=ts.KERNEL_TC_PAIR)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5])
 def test_full_size_every_kernel_on_sampled_pairs(ts, cuda_device, kernel):
     """Every attention kernel on the full bench workload, checked on sampled pairs."""
     w = gen.get("c4_llama3_70b_bf16_greedy")
@@ -242,7 +243,7 @@ def test_full_size_every_kernel_on_sampled_pairs(ts, cuda_device, kernel):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("kernel", [2, 3, 4])
+@pytest.mark.parametrize("kernel", [2, 3, 4, 5])
 @pytest.mark.parametrize("splits", [1, 0])
 def test_tensor_core_kernels_flag_bad_lengths_and_pages(ts, cuda_device, kernel, splits):
     """An invalid sequence gets zero rows (written by the kernel itself with one split, by
@@ -270,3 +271,32 @@ def test_tensor_core_kernels_flag_bad_lengths_and_pages(ts, cuda_device, kernel,
                         kernel=kernel, num_splits=splits, workspace=ws)
     torch.cuda.synchronize()
     assert ts.read_status(ws) & 2
+
+
+@pytest.mark.parametrize("batch,prefix", [(1, [8192]), (2, [8192, 0]), (3, [300, 5000, 17]), (5, [64, 1, 4096, 2048, 63])])
+def test_persistent_kernel_cuts_units_into_pieces(ts, cuda_device, batch, prefix):
+    """Few sequences on 152 SMs: every (sequence, kv head, row-block pair) unit is cut into
+    several pieces whose partials the last piece merges; ragged lengths move the cuts."""
+    w = gen.get("c4_llama3_70b_bf16_greedy")
+    rng = np.random.default_rng(batch)
+    parents = np.stack([trees.random_recursive(rng, w.num_nodes) for _ in range(batch)])
+    w2, x = _custom("c4_llama3_70b_bf16_greedy", parents, prefix)
+    out = run(ts, x, cuda_device, kernel=ts.KERNEL_TC_STREAM)
+    assert_attention_close(out, oracle_attention(x), w2.dtype)
+    out2 = run(ts, x, cuda_device, kernel=ts.KERNEL_TC_STREAM)          # counters reset for the next call
+    assert torch.equal(out, out2)
+
+
+def test_persistent_kernel_with_every_sequence_invalid(ts, cuda_device):
+    w = gen.get("c4_llama3_70b_bf16_greedy").with_batch(3)
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    prob = ts.attn_problem(d["q"], d["k_pages"], d["page_table"], kernel=ts.KERNEL_TC_STREAM)
+    ws = torch.empty(ts.attn_workspace_bytes(prob), dtype=torch.uint8, device=cuda_device)
+    out = torch.full_like(d["q"], 7.0)
+    bad = torch.full_like(d["prefix_lens"], 10 ** 6)
+    ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], bad, d["tree_parents"], out,
+                        kernel=ts.KERNEL_TC_STREAM, workspace=ws)
+    torch.cuda.synchronize()
+    assert ts.read_status(ws) & 4
+    assert torch.all(out == 0)

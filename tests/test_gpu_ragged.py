@@ -25,7 +25,7 @@ SIZES = [64, 17, 1, 40]
 PREFIX = [100, 37, 0, 300]
 
 
-@pytest.mark.parametrize("kernel,splits", [(1, 1), (1, 0), (2, 1), (2, 0), (3, 1), (3, 0), (4, 1), (4, 0)])
+@pytest.mark.parametrize("kernel,splits", [(1, 1), (1, 0), (2, 1), (2, 0), (3, 1), (3, 0), (4, 1), (4, 0), (5, 0)])
 def test_attention_over_trees_of_different_sizes(ts, cuda_device, kernel, splits):
     """Present rows match the oracle, padding rows are zero, and no page past a tree's
     own S + N_b tokens is read (those page ids are made invalid)."""
@@ -50,7 +50,7 @@ def test_attention_over_trees_of_different_sizes(ts, cuda_device, kernel, splits
         assert torch.all(out[b, n:] == 0)
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5])
 def test_attention_over_trees_of_up_to_128_nodes_of_different_sizes(ts, cuda_device, kernel):
     """A batch of 128-node rows holding trees of 128, 65, 64 and 3 nodes."""
     from dataclasses import replace

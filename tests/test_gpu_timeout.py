@@ -30,7 +30,7 @@ def ts():
     mod.set_wait_limit_ns(0)
 
 
-@pytest.mark.parametrize("kernel,splits", [(2, 1), (3, 1), (2, 0), (4, 1), (4, 0)])
+@pytest.mark.parametrize("kernel,splits", [(2, 1), (3, 1), (2, 0), (4, 1), (4, 0), (5, 0)])
 def test_a_wait_that_runs_out_is_reported_and_the_next_call_is_exact(ts, cuda_device, kernel, splits):
     w = gen.get("c4_llama3_70b_bf16_greedy").with_batch(2)
     x = gi.make_inputs(w, with_accept=False)
