@@ -19,13 +19,17 @@
 //                every row up front (argmax; or max, sum of exp and the sibling Z chain),
 //                then accept_walk (one CTA per sequence) walks on those scalars and draws
 //                the bonus token.  Best when there are few rows (small batch).
-//   path only -- accept_path (one CTA per sequence) walks depth by depth and reduces
-//                only the rows it visits, plus one residual pass per rejected sibling
-//                that has a successor; it reads about (accepted + 1) rows per sequence
-//                instead of N.
-// Row passes use float4 loads when the vocabulary is a multiple of 4, compensated
-// float sums per thread and float64 across threads; the bonus draw scans one row with
-// float terms and float64 running sums.
+//   path only -- walks depth by depth and reduces only the rows it visits, plus one
+//                residual pass per rejected sibling that has a successor; it reads about
+//                (accepted + 1) rows per sequence instead of N.  accept_cluster (the
+//                default for float4 rows up to 131072 tokens) holds a row in the
+//                registers of one thread-block cluster per sequence, takes the softmax
+//                max and sum in one cluster round, stages the draft row in shared memory
+//                at its first pass, and draws the bonus token from float32 prefix sums;
+//                accept_path (one CTA per sequence) covers the other shapes.
+// The all-rows kernels and accept_path use float4 loads when the vocabulary is a multiple
+// of 4, compensated float sums per thread and float64 across threads; their bonus draw
+// scans one row with float terms and float64 running sums.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
