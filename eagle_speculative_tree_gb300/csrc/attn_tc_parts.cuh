@@ -141,6 +141,11 @@ template <int TILE>
 __device__ __forceinline__ void tile_mask(uint32_t (&mw)[TILE / 32], int base, int S, int t1, uint64_t anc0,
                                           uint64_t anc1, bool row_ok) {
     const int pref_end = min(S, t1) - base;
+    if (pref_end >= TILE) {                             // a tile of prefix tokens only
+#pragma unroll
+        for (int w = 0; w < TILE / 32; ++w) mw[w] = row_ok ? 0xffffffffu : 0u;
+        return;
+    }
     const int tree_lo = S - base, tree_hi = t1 - base;
 #pragma unroll
     for (int w = 0; w < TILE / 32; ++w) {
@@ -198,6 +203,45 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&v)[TILE], const uint32_t
         else add_f32x2(a0, a1, p0, p1);
     }
     l += (a0 + a1) + (a2 + a3);
+}
+
+// The common case of softmax_tile, without the row maximum: P = 2^(s * sc - m_used) against
+// the running max in use, and `ts` the tile's sum of P.  The result equals softmax_tile's
+// whenever no element of the tile exceeds m_used + 8 (then softmax_tile keeps m_used), and
+// a sum of at most 2^8 shows exactly that; false otherwise (also while m_used is -inf and
+// the row sees a column), and then v holds partial results: the caller reloads S and calls
+// softmax_tile.  Skipping the maximum removes half an instruction per element and the
+// maximum -> exponential dependency from nearly every tile.
+template <int TILE>
+__device__ __forceinline__ bool softmax_tile_fast(uint32_t (&v)[TILE], const uint32_t (&mw)[TILE / 32], bool full,
+                                                  float sc, float m_used, float& ts) {
+    ts = 0.f;
+    if (m_used == -INFINITY) {                          // no column seen yet
+        uint32_t seen = 0u;
+#pragma unroll
+        for (int w = 0; w < TILE / 32; ++w) seen |= mw[w];
+        if (seen) return false;                         // the first visible column: the exact path sets the max
+#pragma unroll
+        for (int c = 0; c < TILE / 2; ++c) v[c] = 0u;   // nothing visible: P = 0
+        return true;
+    }
+    if (!full) {
+        constexpr uint32_t kNegInf = 0xff800000u;
+#pragma unroll
+        for (int c = 0; c < TILE; ++c) v[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? v[c] : kNegInf;
+    }
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int c = 0; c < TILE / 2; ++c) {
+        float x0, x1;
+        fma_f32x2(x0, x1, __uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]), sc, -m_used);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        v[c] = pack_bf16x2(p0, p1);
+        if (c & 1) add_f32x2(a2, a3, p0, p1);
+        else add_f32x2(a0, a1, p0, p1);
+    }
+    ts = (a0 + a1) + (a2 + a3);
+    return ts <= 256.f;                                 // false for inf / NaN too
 }
 
 // O (128 fp32 columns of this thread's lane, from `ocol`) *= f; the whole warp takes part.
