@@ -388,9 +388,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) tmem_ld32(scol + c * 32, v + c * 32);
                 tmem_wait_ld();
             }
-            bool resc;
-            float alpha;
-            tcparts::softmax_tile<kBN>(v, mw, full, sc, m_used, l, resc, alpha);
+            bool resc = false;
+            float alpha = 1.f, ts;
+            if (__all_sync(0xffffffffu, tcparts::softmax_tile_fast<kBN>(v, mw, full, sc, m_used, ts))) {
+                l += ts;                                     // no row's max moved past m_used + 8
+            } else {                                         // S again, and the exact path
+                if (warp_rows) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(scol + c * 32, v + c * 32);
+                    tmem_wait_ld();
+                }
+                tcparts::softmax_tile<kBN>(v, mw, full, sc, m_used, l, resc, alpha);
+            }
             // the P buffer and O are free once P_{j-1} V_{j-1} has completed
             if (j > 0 && !wait_bar(&bars->pv_done, (j - 1) & 1, p.wait_ns)) {
                 alive = false;
