@@ -417,10 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // commits.  g counts the KV tiles over the CTA's life (ring stages, S buffers and
         // their phases); k counts the ranges (Q, O and their phases).
         const int t = warp - kWarpMma;
-        auto ready = [&](uint64_t* x, uint32_t px) -> bool {
-            bool r = mbar_try_wait(x, px);
-            if (!__all_sync(0xffffffffu, r)) r = !*abort_flag && (r || mbar_wait_bounded(x, px, p.wait_ns));
-            return __all_sync(0xffffffffu, r);
+        auto ready = [&](uint64_t* x, uint32_t px) -> bool {     // polled: its wake-ups are on the critical path
+            const uint64_t t0 = global_ns();
+            for (;;) {
+                if (__all_sync(0xffffffffu, mbar_test_wait(x, px))) return true;
+                if (*abort_flag || global_ns() - t0 > p.wait_ns) return false;
+            }
         };
         constexpr uint32_t kIdS = idesc_bf16_f32(128, kBN, false);
         constexpr uint32_t kIdO = idesc_bf16_f32(128, 128, true);
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t mw[kBN / 32];
             tcparts::tile_mask<kBN>(mw, u.t0 + j * kBN, u.S, u.t1, u.anc0, u.anc1, u.ok);
             const bool full = __all_sync(0xffffffffu, (mw[0] & mw[1]) == 0xffffffffu);
-            if (!mbar_wait_bounded(&bars->s_full[t][bf], (gj >> 1) & 1, p.wait_ns)) return false;
+            if (!mbar_wait_spin(&bars->s_full[t][bf], (gj >> 1) & 1, p.wait_ns)) return false;
             tc_fence_after();
             if (kStream && tq >= 0) issue_q(tq);
             if (warp_rows) {
