@@ -136,14 +136,16 @@ AttnPlan make_plan(const treespec_attn_shape& s, int sms) {
     if (s.num_splits > 0) {
         splits = s.num_splits;
     } else if (tc) {
-        // One CTA fits an SM.  Split a sequence only as far as filling the SMs once needs,
-        // keep a CTA's run at most 66 tiles (a ragged batch's longest sequences split into
-        // several CTAs; an 8256-token one stays whole), and no chunk below two tiles: each
-        // split costs a pipeline fill and its partials.  Measured against the previous rule
-        // (about two CTAs per SM): 32 x 8192 tokens at batch 8 0.147 ms against 0.192 ms,
-        // 8 x 4096 tokens (32 kv heads) 0.116 against 0.131, 64 ragged sequences up to 32768
-        // tokens 0.751 against 0.774.
-        splits = (sms + units - 1) / units;
+        // One CTA fits an SM.  Split a sequence only as far as one wave of CTAs holds
+        // (rounded down: a few CTAs past the SM count would run as a second wave), keep a
+        // CTA's run at most 66 tiles (a ragged batch's longest sequences split into several
+        // CTAs; an 8256-token one stays whole), and no chunk below two tiles: each split
+        // costs a pipeline fill and its partials.  Measured against earlier rules: about two
+        // CTAs per SM gave 32 x 8192 tokens at batch 8 0.192 ms against 0.147, 8 x 4096
+        // tokens (32 kv heads) 0.131 against 0.116, 64 ragged sequences up to 32768 tokens
+        // 0.774 against 0.751; rounding up gave the 64 q / 8 kv-head, 64-node shape 0.056 ms
+        // at batch 1 (160 CTA-pair CTAs) against 0.044 (128) and 0.077 at batch 2 against 0.058.
+        splits = units >= sms ? 1 : sms / units;
         const long long cap = 66ll * tile;
         splits = std::max(splits, (max_tokens + cap - 1) / cap);
         splits = std::min(splits, std::max(1ll, (max_tokens + 2 * tile - 1) / (2 * tile)));
