@@ -633,8 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY, l = 0.f;
             {
                 const bool wr = __any_sync(0xffffffffu, RA.ok);
-                for (int j = 0; alive && j < RA.ntiles; ++j)
-                    alive = tile(RA, wr, j, g + j, m_used, l, (haveB && j == RA.ntiles - 1) ? TB : -1);
+                // the last tile apart: only it copies the next range's Q in, so the loop's
+                // instance of the tile carries no copy
+                for (int j = 0; alive && j + 1 < RA.ntiles; ++j) alive = tile(RA, wr, j, g + j, m_used, l, -1);
+                if (alive) alive = tile(RA, wr, RA.ntiles - 1, g + RA.ntiles - 1, m_used, l, haveB ? TB : -1);
             }
             if (!alive) break;
             g += RA.ntiles;
