@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(sm + C::kOffMisc + 4);
     uint64_t* anc_s = reinterpret_cast<uint64_t*>(sm + C::kOffAnc);
+    grid_dep_wait();                               // the prologue's ancestor words, lengths and counts
 
     // One CTA: grid (split, kv head x row block, sequence).  Pair: grid (split x 2 + rank,
     // kv head x pair of row blocks, sequence) with clusters of two along x -- the
@@ -487,13 +488,15 @@ static cudaError_t launch_tc(const AttnParams& p, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;                    // the two row blocks of a pair
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;                    // the two row blocks of a pair
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = kPair ? 1 : 0;
+    cfg.numAttrs = kPair ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, p, mk, mv);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

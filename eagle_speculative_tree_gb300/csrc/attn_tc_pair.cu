@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t* abort_flag = reinterpret_cast<uint32_t*>(sm + kOffMisc + 4);
     uint64_t* anc_s = reinterpret_cast<uint64_t*>(sm + kOffAnc);
     int* tcum = reinterpret_cast<int*>(sm + kOffAnc);
+    grid_dep_wait();                               // the prologue's ancestor words, lengths, counts and flags
 
     const int pairs = p.row_blocks / kNQ;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -717,7 +718,18 @@ cudaError_t launch_two_tile(const AttnParams& p, cudaStream_t s, dim3 grid) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_pair_kernel<kStream>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    attn_tc_pair_kernel<kStream><<<grid, kThreads, kSmemBytes, s>>>(p, mk, mv);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_tc_pair_kernel<kStream>, p, mk, mv);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -24,6 +24,15 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Programmatic dependent launch between the tree prologue and the attention kernel that
+// follows it on the stream.  The prologue lets the next grid launch at once; the
+// attention kernel, launched with the programmatic-serialisation attribute, waits at its
+// first instruction until the prologue has finished and its writes are visible, so only
+// the launch and the CTAs' start overlap the prologue.  Launched without the attribute,
+// the wait returns at once.
+__device__ __forceinline__ void grid_dep_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // bf16 <-> f32 on raw bit patterns (bf16 is the high half of an f32).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -18,6 +18,7 @@ namespace treespec {
 __global__ void __launch_bounds__(kMaxNodes) tree_prologue_kernel(AttnParams p) {
     __shared__ int par[kMaxNodes];
     __shared__ int bad, first_pad;
+    grid_dep_release();                   // the attention kernel may launch; it waits for this grid
     const int b = blockIdx.x, i = threadIdx.x, N = p.N;
     if (i == 0) {
         bad = 0;

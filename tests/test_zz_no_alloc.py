@@ -72,6 +72,24 @@ def test_noalloc_matches_workspace_entry_point_twice(ts, cuda_device, name):
         _close(out, ref, w.dtype)
 
 
+def test_noalloc_runs_the_one_range_kernel_where_the_persistent_one_does_not_fit(ts, cuda_device):
+    """At the full Llama-3-70B batch the automatic plan is the persistent two-tile kernel,
+    whose partial slots exceed the fixed array: the no-allocation entry runs the two-tile
+    kernel one range per CTA instead, and agrees with the workspace entry point."""
+    w = gen.get("c4_llama3_70b_bf16_greedy")
+    x = gi.make_inputs(w, with_accept=False)
+    d = attn_device_inputs(x, cuda_device)
+    prob = ts.attn_problem(d["q"], d["k_pages"], d["page_table"])
+    assert ts.attn_plan(prob).kernel == ts.KERNEL_TC_STREAM
+    assert ts.attn_workspace_bytes(prob) > 32 << 20
+    ref = ts.tree_attn_verify(d["q"], d["k_pages"], d["v_pages"], d["page_table"], d["prefix_lens"],
+                              d["tree_parents"])
+    out = torch.full_like(d["q"], float("nan"))
+    assert _noalloc(ts, d, out, prob) == 0
+    torch.cuda.synchronize()
+    _close(out, ref, w.dtype)
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(ts, cuda_device):
     w = gen.get("c4_llama3_70b_bf16_greedy@b1")
     x = gi.make_inputs(w, with_accept=False)
