@@ -484,11 +484,11 @@ extern "C" int tree_draft_step(const float* logprobs, int32_t batch, int32_t fro
     p.step = step;
     p.M = max_nodes;
     // A row's vocabulary is cut into S parts (one CTA each) only where the rows alone would
-    // leave SMs idle: each warp's list filters best over a long stream (its k-th entry
-    // rises and fewer groups pass the vote), so parts cost more than they save once every
-    // SM has a row (measured: 64 rows of 8 frontier nodes x 128256 tokens took 58 us per
-    // step in one part, more in three).  No part below 8192 tokens, parts a multiple of
-    // 1024 tokens.
+    // leave SMs idle: a CTA's lists filter best over a long stream (the floor rises and
+    // fewer groups pass the vote), so parts cost more than they save once every SM has a
+    // row (measured per step over 128256 tokens: 256 rows 36 us in one part, 41 in two;
+    // 64 rows 23 us in one, 19 in two, 21 in four).  No part below 8192 tokens, parts a
+    // multiple of 1024 tokens.
     {
         const long long rows = (long long)batch * frontier;
         long long S = sm_count_or_default() / rows;

@@ -19,26 +19,42 @@ namespace treespec {
 
 namespace {
 
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 512;
 
 // a ranks before b: larger value, or equal value and smaller index
 __device__ __forceinline__ bool before(float av, int at, float bv, int bt) {
     return av > bv || (av == bv && at < bt);
 }
 
+// Order-preserving map of a float onto int (for atomicMax on shared memory): x < y iff
+// key(x) < key(y), for every float but NaN.
+__device__ __forceinline__ int order_key(float x) {
+    const int b = __float_as_int(x);
+    return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float from_order_key(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
 // Top-k tokens of one part of a frontier row (a row's vocabulary is cut into p.S parts
 // of p.chunk tokens, one CTA each, so that the SMs share every row: one CTA per row left
 // most of them idle).  Each warp keeps one sorted list spread over its lanes (lane i
 // holds rank i, i < k) and a copy of its k-th entry in every lane; the lanes test their
 // elements against that threshold with one ballot, and the rare winners are inserted one
-// at a time by shifting the list down a lane.  Then warp 0 ranks the warps' lists.  (With
-// a private list per thread, some lane of a warp inserts at almost every element and the
-// warp runs the insertion nearly always.)
+// at a time by shifting the list down a lane.  (With a private list per thread, some
+// lane of a warp inserts at almost every element and the warp runs the insertion nearly
+// always.)  The warps also share a floor in shared memory, below which no element can be
+// in the row's top k: the largest of their lists' k-th values (that warp's k entries beat
+// anything below it), and at the start the k-th largest of each warp's lane maxima over
+// its first batch (k distinct elements are at or above it).  Elements equal to the floor
+// are still looked at (their token decides).  Without the seed a warp's first batch met
+// an empty list and all 32 lanes' elements went in one by one.  At the end the CTA ranks
+// the list entries at or above the floor.
 template <bool VEC>
 __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftParams p) {
     constexpr int kWarps = kTopkThreads / 32;
     __shared__ float sv[kWarps * kMaxTopk];
     __shared__ int st[kWarps * kMaxTopk];
+    __shared__ int floor_key;                            // order_key of the warps' largest k-th value
+    __shared__ int n_cand;
     const int row = blockIdx.x / p.S, part = blockIdx.x % p.S;   // row = b * F + f
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = p.k;
@@ -46,8 +62,38 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
     const float* lp = p.logprobs + size_t(row) * p.V;
     float wv = -INFINITY, tv = -INFINITY;                // this lane's list entry; the warp's k-th entry
     int wt = INT_MAX, tt = INT_MAX;
+    if (tid == 0) floor_key = order_key(-INFINITY);
+    __syncthreads();
+    float fl = -INFINITY;                                 // this warp's last look at the floor
+    auto look = [&]() {                                   // publish this warp's k-th value, read the floor
+        if (tv > fl) {
+            if (lane == 0) atomicMax(&floor_key, order_key(tv));
+            fl = tv;
+        }
+        fl = fmaxf(fl, from_order_key(*reinterpret_cast<volatile int*>(&floor_key)));
+    };
+    // The k-th largest of the lanes' maxima over a batch (a bitonic sort across the warp,
+    // largest first): k distinct elements are at or above it, so it is a floor too.
+    // Without it a warp's first batch meets an empty list, every lane wins the ballot,
+    // and the winners go in one at a time.
+    auto seed = [&](float lm) {
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                const float o = __shfl_xor_sync(0xffffffffu, lm, stride);
+                const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+                lm = keep_max ? fmaxf(lm, o) : fminf(lm, o);
+            }
+        }
+        const float kth = __shfl_sync(0xffffffffu, lm, k - 1);
+        if (kth > fl) {
+            if (lane == 0) atomicMax(&floor_key, order_key(kth));
+            fl = kth;
+        }
+    };
     auto consider = [&](float x, int t) {                 // called by all lanes together
-        unsigned m = __ballot_sync(0xffffffffu, before(x, t, tv, tt));
+        unsigned m = __ballot_sync(0xffffffffu, x >= fl && before(x, t, tv, tt));
         while (m) {
             const int src = __ffs(m) - 1;
             m &= m - 1;
@@ -75,6 +121,7 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
     // CTA latency-bound at about 10 GB/s)
     constexpr int kU = 8;
     if constexpr (VEC) {                                  // p.chunk is a multiple of 4
+        bool first = true;
         for (int v0 = v_lo; v0 < v_hi; v0 += kTopkThreads * 4 * kU) {
             float4 x[kU];
 #pragma unroll
@@ -83,12 +130,20 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
                 x[u] = v < v_hi ? __ldg(reinterpret_cast<const float4*>(lp + v))
                                 : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
+            if (first) {                                  // the warp's first batch seeds the floor
+                float lm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) lm = fmaxf(lm, fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)));
+                seed(lm);
+                first = false;
+            }
+            look();
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 // one vote per float4: only a group holding a value at or above the warp's
                 // k-th entry can change the list (exact: a tie needs the token test below)
                 const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
-                if (!__any_sync(0xffffffffu, m4 >= tv)) continue;
+                if (!__any_sync(0xffffffffu, m4 >= fmaxf(tv, fl))) continue;
                 const int v = v0 + (u * kTopkThreads + tid) * 4;
                 const bool in = v < v_hi;
                 consider(x[u].x, in ? v : INT_MAX);
@@ -98,6 +153,7 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
             }
         }
     } else {
+        bool first = true;
         for (int v0 = v_lo; v0 < v_hi; v0 += kTopkThreads * kU) {
             float x[kU];
 #pragma unroll
@@ -105,6 +161,14 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
                 const int v = v0 + u * kTopkThreads + tid;
                 x[u] = v < v_hi ? __ldg(lp + v) : -INFINITY;
             }
+            if (first) {
+                float lm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) lm = fmaxf(lm, x[u]);
+                seed(lm);
+                first = false;
+            }
+            look();
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int v = v0 + u * kTopkThreads + tid;
@@ -112,24 +176,34 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
             }
         }
     }
-    if (lane < k) {
-        sv[warp * kMaxTopk + lane] = wv;
-        st[warp * kMaxTopk + lane] = wt;
+    // The part's top k are among the list entries at or above the final floor (an entry
+    // below it has the k entries of the floor's warp ahead of it): gather those, then rank
+    // each against the others, all threads at once.  Ranks break equal (value, token)
+    // pairs -- only the (-inf, INT_MAX) fillers of a part shorter than k -- by slot.
+    look();
+    __syncthreads();
+    const float fin = from_order_key(floor_key);
+    if (tid == 0) n_cand = 0;
+    __syncthreads();
+    if (lane < k && wv >= fin) {
+        const int c = atomicAdd(&n_cand, 1);
+        sv[c] = wv;
+        st[c] = wt;
     }
     __syncthreads();
-    if (warp == 0) {                                      // rank the kWarps * k entries
-        const int n = kWarps * k;
-        for (int c = lane; c < n; c += 32) {
-            const int ci = (c / k) * kMaxTopk + c % k;
-            int rank = 0;
-            for (int o = 0; o < n; ++o) {
-                const int oi = (o / k) * kMaxTopk + o % k;
-                rank += before(sv[oi], st[oi], sv[ci], st[ci]) ? 1 : 0;
-            }
-            if (rank < k) {                               // a part shorter than k leaves INT_MAX entries
-                p.tk_tok[size_t(blockIdx.x) * k + rank] = st[ci];
-                p.tk_lp[size_t(blockIdx.x) * k + rank] = sv[ci];
-            }
+    const int n = n_cand;
+    for (int c = tid; c < n; c += kTopkThreads) {
+        const float cv = sv[c];
+        const int ct = st[c];
+        int rank = 0;
+        for (int o = 0; o < n; ++o) {
+            const float ov = sv[o];
+            const int ot = st[o];
+            rank += (before(ov, ot, cv, ct) || (ov == cv && ot == ct && o < c)) ? 1 : 0;
+        }
+        if (rank < k) {
+            p.tk_tok[size_t(blockIdx.x) * k + rank] = ct;
+            p.tk_lp[size_t(blockIdx.x) * k + rank] = cv;
         }
     }
 }
