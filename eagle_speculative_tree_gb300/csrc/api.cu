@@ -500,7 +500,7 @@ extern "C" int tree_draft_step(const float* logprobs, int32_t batch, int32_t fro
         p.chunk = int(chunk);
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(p.status, 0, sizeof(uint32_t), st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
+    // the top-k kernel clears the status word (no memset: one stream operation fewer a step)
     if (launch_draft_step(p, st) != cudaSuccess) return TREESPEC_ERR_LAUNCH;
     g_launches += 2;
     return TREESPEC_OK;

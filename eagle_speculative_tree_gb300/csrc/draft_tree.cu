@@ -55,8 +55,10 @@ __global__ void __launch_bounds__(kTopkThreads) draft_topk_kernel(const DraftPar
     __shared__ int st[kWarps * kMaxTopk];
     __shared__ int floor_key;                            // order_key of the warps' largest k-th value
     __shared__ int n_cand;
+    grid_dep_release();                                   // the select kernel may launch; it waits for this grid
     const int row = blockIdx.x / p.S, part = blockIdx.x % p.S;   // row = b * F + f
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (blockIdx.x == 0 && tid == 0) *p.status = 0;       // only the select kernel after this grid sets bits
     const int k = p.k;
     const int v_lo = part * p.chunk, v_hi = min(p.V, v_lo + p.chunk);
     const float* lp = p.logprobs + size_t(row) * p.V;
@@ -216,6 +218,7 @@ __global__ void __launch_bounds__(kSelectThreads) draft_select_kernel(const Draf
     __shared__ float cs[kMaxFrontier * kMaxTopk];
     __shared__ float mv[kMaxFrontier * kMaxTopk];
     __shared__ int mt[kMaxFrontier * kMaxTopk];
+    grid_dep_wait();                                      // every part's list, and the cleared status word
     const int b = blockIdx.x, tid = threadIdx.x;
     const int k = p.k, F = p.F, S = p.S, nc = F * k;
     int* par = p.node_parent + size_t(b) * p.M;
@@ -329,7 +332,18 @@ cudaError_t launch_draft_step(const DraftParams& p, cudaStream_t s) {
     if (p.V % 4 == 0) draft_topk_kernel<true><<<grid, kTopkThreads, 0, s>>>(p);
     else draft_topk_kernel<false><<<grid, kTopkThreads, 0, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-    draft_select_kernel<<<unsigned(p.B), kSelectThreads, 0, s>>>(p);
+    // launched as a programmatic dependent of the top-k grid: only its launch overlaps it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.B));
+    cfg.blockDim = dim3(kSelectThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, draft_select_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -57,6 +57,8 @@ def build_both(ts, device, B, V, k, steps, N, seed, ties=False):
     (3, 1001, 16, 2, 24),       # scalar loads (V % 4 != 0), the largest branching
     (2, 5003, 1, 7, 8),         # topk 1: the greedy chain
     (2, 32000, 8, 6, 128),      # a 128-node tree: two ancestor words per node downstream
+    (32, 128256, 8, 2, 64),     # 256 frontier rows of the Llama-3 vocabulary, one part each
+    (8, 128256, 8, 2, 64),      # 64 such rows, two parts each
 ])
 @pytest.mark.parametrize("ties", [False, True])
 def test_draft_tree_matches_oracle(ts, cuda_device, B, V, k, steps, N, ties):
