@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kSelectThreads) draft_select_kernel(const Draf
         const float ev = p.tk_lp[e0 + e];
         const int et = p.tk_tok[e0 + e];
         int rank = 0;
+#pragma unroll 8
         for (int o = f * S * k; o < (f + 1) * S * k; ++o) rank += before(p.tk_lp[e0 + o], p.tk_tok[e0 + o], ev, et) ? 1 : 0;
         if (rank < k) {
             mv[f * k + rank] = ev;
@@ -253,7 +254,9 @@ __global__ void __launch_bounds__(kSelectThreads) draft_select_kernel(const Draf
     __syncthreads();
     for (int c = tid; c < nc; c += kSelectThreads) {
         int rank = 0;
-        for (int o = 0; o < nc; ++o) rank += before(cs[o], o, cs[c], c) ? 1 : 0;
+        const float cc = cs[c];
+#pragma unroll 8
+        for (int o = 0; o < nc; ++o) rank += before(cs[o], o, cc, c) ? 1 : 0;
         if (rank < k) p.frontier_out[size_t(b) * k + rank] = base + c;
     }
     if (p.step == 0 && tid == 0) {
@@ -266,7 +269,9 @@ __global__ void __launch_bounds__(kSelectThreads) draft_select_kernel(const Draf
 // One CTA per sequence: keep the root and the N - 1 best eligible nodes (every node, or
 // the pool's), numbered by original index, parents remapped; a pool with fewer eligible
 // nodes leaves the rest of the row as padding (parent kAbsent, token -1).
-__global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
+constexpr int kRerankThreads = 256;
+__global__ void __launch_bounds__(kRerankThreads) rerank_kernel(const RerankParams p) {
+    __shared__ int wsum[kRerankThreads / 32];
     __shared__ float s[kMaxDraftNodes];
     __shared__ int par[kMaxDraftNodes];
     __shared__ int kept[kMaxDraftNodes], newidx[kMaxDraftNodes];
@@ -290,17 +295,41 @@ __global__ void __launch_bounds__(256) rerank_kernel(const RerankParams p) {
         }
         __syncthreads();
     }
-    for (int i = tid; i < M; i += blockDim.x) {
+    for (int i = tid; i < M; i += kRerankThreads) {
         int rank = 0;
-        if (elig[i])
-            for (int j = 1; j < M; ++j) rank += (elig[j] && before(s[j], j, s[i], i)) ? 1 : 0;
+        if (elig[i]) {
+            const float si = s[i];
+#pragma unroll 8
+            for (int j = 1; j < M; ++j) rank += (elig[j] && before(s[j], j, si, i)) ? 1 : 0;
+        }
         kept[i] = i == 0 || (elig[i] && rank < N - 1);
     }
     __syncthreads();
-    for (int i = tid; i < M; i += blockDim.x) {
-        int n = 0;
-        for (int j = 0; j < i; ++j) n += kept[j];
-        newidx[i] = n;                                    // root -> 0, kept nodes -> 1, 2, ...
+    {   // newidx = the kept nodes before i (root -> 0, kept nodes -> 1, 2, ...): a block scan,
+        // four consecutive nodes a thread
+        static_assert(kRerankThreads * 4 >= kMaxDraftNodes, "four nodes a thread cover the arrays");
+        const int lane = tid & 31, warp = tid >> 5, i0 = tid * 4;
+        int c[4], run = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            c[e] = i0 + e < M ? kept[i0 + e] : 0;
+            run += c[e];
+        }
+        int inc = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) wsum[warp] = inc;
+        __syncthreads();
+        int ex = inc - run;
+        for (int w = 0; w < warp; ++w) ex += wsum[w];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (i0 + e < M) newidx[i0 + e] = ex;
+            ex += c[e];
+        }
     }
     __syncthreads();
     const int nk = newidx[M - 1] + kept[M - 1];           // nodes kept, root included
@@ -348,7 +377,7 @@ cudaError_t launch_draft_step(const DraftParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_rerank(const RerankParams& p, cudaStream_t s) {
-    rerank_kernel<<<unsigned(p.B), 256, 0, s>>>(p);
+    rerank_kernel<<<unsigned(p.B), kRerankThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
