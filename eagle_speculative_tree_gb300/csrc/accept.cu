@@ -400,6 +400,25 @@ __device__ __forceinline__ uint32_t check_parents(const int* par, int N) {
     return st;
 }
 
+// The children of every node in ascending index, as the walks test them: kid0[c] is the
+// smallest k > c with par[k] == c and sib[c] the smallest k > c with par[k] == par[c]
+// (-1: none), so the children of c are kid0[c], sib[kid0[c]], ...  The same nodes a scan
+// of par from c + 1 finds, in O(1) per test instead of O(N) for one thread while the CTA
+// waits at the next barrier.  Threads c < N of the block, one node each.
+__device__ __forceinline__ void child_tables(const int* par, int N, int* kid0, int* sib, int tid, int nt) {
+    for (int c = tid; c < N; c += nt) {
+        const int pc = par[c];
+        int k0 = -1, sb = -1;
+        for (int k = c + 1; k < N && (k0 < 0 || sb < 0); ++k) {
+            const int pk = par[k];
+            if (k0 < 0 && pk == c) k0 = k;
+            if (sb < 0 && pk == pc) sb = k;
+        }
+        kid0[c] = k0;
+        sib[c] = sb;
+    }
+}
+
 // ------------------------------------------------------------ all-rows schedule
 
 template <int NT, bool VEC, bool STOCH>
@@ -514,6 +533,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
     __shared__ float redf[32];
     __shared__ int redi[32];
     __shared__ int s_cur, s_len, s_action, s_child;
+    __shared__ int kid0[kMaxNodes], sib[kMaxNodes];
     const int b = blockIdx.x, tid = threadIdx.x;
     const int N = p.N, V = p.V;
     for (int c = tid; c < N; c += NT) {
@@ -521,6 +541,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
         tok[c] = p.tokens[size_t(b) * N + c];
     }
     __syncthreads();
+    child_tables(par, N, kid0, sib, tid, NT);
     uint32_t st = 0;
     if (tid == 0) {
         st = check_parents(par, N);
@@ -546,9 +567,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
         int jj = 0, pos = cur, action = 0, child = -1;
         for (;;) {
             if (tid == 0) {
-                int nc = -1;
-                for (int k = pos + 1; k < N; ++k)
-                    if (par[k] == cur) { nc = k; break; }
+                const int nc = pos == cur ? kid0[cur] : sib[pos];
                 int act = 0;                              // 0: no child left
                 if (nc >= 0) {
                     const int x = tok[nc];
@@ -567,9 +586,7 @@ __global__ void __launch_bounds__(NT) accept_path_kernel(AcceptParams p) {
                     if (ok) {
                         act = 1;                          // accepted
                     } else {
-                        int more = -1;
-                        for (int k = nc + 1; k < N; ++k)
-                            if (par[k] == cur) { more = k; break; }
+                        const int more = sib[nc];
                         act = more >= 0 ? 2 : 3;          // rejected; 2: a sibling follows
                     }
                 }
@@ -767,6 +784,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
     __shared__ int redi[32];
     __shared__ int s_cur, s_len, s_action, s_child, s_found;
     __shared__ float ch_lg[kMaxNodes], ch_q[kMaxNodes];     // target logit / draft prob of each child's token
+    __shared__ int kid0[kMaxNodes], sib[kMaxNodes];
     __shared__ ClusterRed<CL> cred;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
@@ -846,6 +864,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             if (v < V) x = __ldg(reinterpret_cast<const float4*>(lg + v));
             r[e] = x.x; r[e + 1] = x.y; r[e + 2] = x.z; r[e + 3] = x.w;
         }
+        if (depth == 0) {                                   // while the root's row is in flight
+            child_tables(par, N, kid0, sib, tid, NT);
+            __syncthreads();
+        }
         if constexpr (!STOCH) {
             float best = -INFINITY;
             int bi = 0x7fffffff;
@@ -878,9 +900,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         int jj = 0, pos = cur, action = 0, child = -1;
         for (;;) {
             if (tid == 0) {
-                int nc = -1;
-                for (int k = pos + 1; k < N; ++k)
-                    if (par[k] == cur) { nc = k; break; }
+                const int nc = pos == cur ? kid0[cur] : sib[pos];
                 int act = 0;
                 if (nc >= 0) {
                     const int x = tok[nc];
@@ -899,9 +919,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
                     if (ok) {
                         act = 1;
                     } else {
-                        int more = -1;
-                        for (int k = nc + 1; k < N; ++k)
-                            if (par[k] == cur) { more = k; break; }
+                        const int more = sib[nc];
                         act = more >= 0 ? 2 : 3;
                     }
                 }
