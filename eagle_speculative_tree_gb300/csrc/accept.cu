@@ -894,9 +894,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             const float2 ms = red.maxsum(mloc, (ls[0] + ls[1]) + (ls[2] + ls[3]));
             M2 = ms.x;
             invS = 1.f / ms.y;
+            // r = p (the row's probabilities) is formed only where it is used -- the residual
+            // after a rejection and the bonus draw where the walk stops -- not at a node whose
+            // child is accepted (the child tests take p of the child's token from its logit)
+        }
+        bool r_is_p = !STOCH;
+        auto form_p = [&]() {
+            if (r_is_p) return;
 #pragma unroll
             for (int e = 0; e < E; ++e) r[e] = ex2(fmaf(r[e], p.c, -M2)) * invS;   // -inf (padding) -> 0
-        }
+            r_is_p = true;
+        };
         int jj = 0, pos = cur, action = 0, child = -1;
         for (;;) {
             if (tid == 0) {
@@ -936,6 +944,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
             if constexpr (STOCH) {                          // the next sibling sees the residual
                 // the previous sibling's rescale r = max(r - q, 0) / Z is applied here, in the
                 // same pass over q as this residual's mass (same operations, one read of q)
+                form_p();
                 float zs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < E; e += 4) {
@@ -961,6 +970,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1) accept_clust
         }
         if (action != 1) {
             rej = jj;
+            form_p();                                       // the bonus draw reads r
             if (STOCH && piz > 0.f) {                       // the last deferred rescale
 #pragma unroll
                 for (int e = 0; e < E; e += 4) {
