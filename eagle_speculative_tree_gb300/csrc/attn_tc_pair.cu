@@ -94,7 +94,7 @@ constexpr int kOffMisc = kOffBar + int(sizeof(Bars));
 constexpr int kOffAnc = kOffMisc + 16;
 constexpr int kSmemBytes = kOffAnc + kMaxNodes * kAncWords * 8;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert((kStreamMaxBatch + 1) * 4 <= kMaxNodes * kAncWords * 8, "tile offsets fit the ancestor area");
+static_assert((kStreamMaxBatch + 2) * 4 <= kMaxNodes * kAncWords * 8, "tile offsets fit the ancestor area");
 
 // One contiguous range of KV tiles of one unit that a CTA computes.
 struct Seg {
@@ -129,10 +129,11 @@ __device__ __forceinline__ void unit_at(int T, const int* tcum, int B, int Hkv, 
 }
 
 // The sequences' tile offsets (an invalid sequence has no tiles, a valid one at least
-// one), by one warp.
+// one), by one warp; tcum[B + 1] is 1 if some sequence has no tiles.
 __device__ __forceinline__ void tile_offsets(const AttnParams& p, int* tcum) {
     const int lane = threadIdx.x & 31;
     int run = 0;
+    bool empty = false;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
         int n = 0;
@@ -140,6 +141,7 @@ __device__ __forceinline__ void tile_offsets(const AttnParams& p, int* tcum) {
             const int S = p.lens[bb];
             if (S >= 0) n = (S + p.nn[bb] + kBN - 1) / kBN;
         }
+        empty |= __any_sync(0xffffffffu, bb < p.B && n == 0);
         int inc = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -149,13 +151,68 @@ __device__ __forceinline__ void tile_offsets(const AttnParams& p, int* tcum) {
         if (bb < p.B) tcum[bb] = run + inc - n;
         run += __shfl_sync(0xffffffffu, inc, 31);
     }
-    if (lane == 0) tcum[p.B] = run;
+    if (lane == 0) {
+        tcum[p.B] = run;
+        tcum[p.B + 1] = empty ? 1 : 0;
+    }
 }
 
-// The persistent form's cut: CTA c owns global tiles [lo(c), lo(c + 1)).  All positions
-// are below 2^31 (the host checks the batch's tile count).
-__device__ __forceinline__ int st_lo(int c, int W, int G) { return int((long long)c * W / G); }
-__device__ __forceinline__ int st_owner(int T, int W, int G) { return int(((long long)(T + 1) * G - 1) / W); }
+// The persistent form's cut: CTA c owns global tiles [lo(c), lo(c + 1)).  The cut is even
+// in a weighted position, where each unit costs kCutKappa tiles more than its own tiles
+// (about what a piece's epilogue and the restart of the pipeline take), so that a range
+// that touches one unit more holds fewer tiles.  The weighted start of tile T of unit
+// (pr, b, h), tile j0 of n, is pr WP + Hkv (tcum[b] + k b) + h (k + n) + k + j0, with WP
+// the weight of one row-block pair's units.  With a sequence that has no tiles, or ranges
+// too short for the weights, the cut is even in tiles (k = 0).  All positions are below
+// 2^31 (the host checks the batch's tile count); weighted ones are kept in 64 bits.
+constexpr int kCutKappa = 7;
+struct Cut {
+    long long WP, Wt;      // weight of one pair's units; of all units
+    int k;                 // weight of a unit beyond its tiles (0: the plain cut)
+};
+__device__ __forceinline__ long long cut_wb(const int* tcum, int b, int Hkv, int k) {
+    return (long long)Hkv * (tcum[b] + (long long)k * b);
+}
+__device__ __forceinline__ Cut make_cut(const int* tcum, int B, int Hkv, int pairs, int G) {
+    Cut c;
+    c.k = tcum[B + 1] ? 0 : kCutKappa;
+    c.WP = cut_wb(tcum, B, Hkv, c.k);
+    c.Wt = c.WP * pairs;
+    if (c.k && c.Wt < (long long)(c.k + 2) * G) {
+        c.k = 0;
+        c.WP = cut_wb(tcum, B, Hkv, 0);
+        c.Wt = c.WP * pairs;
+    }
+    return c;
+}
+// lo(c): the first tile whose weighted start is at or past c Wt / G
+__device__ __forceinline__ int cut_lo(const Cut& q, const int* tcum, int B, int Hkv, int W, int G, int c) {
+    if (c >= G) return W;
+    if (q.k == 0) return int((long long)c * W / G);
+    const long long X = (long long)c * q.Wt / G;
+    const int pr = int(X / q.WP);
+    const long long rem = X - pr * q.WP;
+    int lo_b = 0, hi_b = B;                         // the last b with cut_wb(b) <= rem
+    while (hi_b - lo_b > 1) {
+        const int mid = (lo_b + hi_b) >> 1;
+        if (cut_wb(tcum, mid, Hkv, q.k) <= rem) lo_b = mid;
+        else hi_b = mid;
+    }
+    const int n = tcum[lo_b + 1] - tcum[lo_b];
+    const long long off = rem - cut_wb(tcum, lo_b, Hkv, q.k);
+    const int h = int(off / (q.k + n));
+    const int x = int(off - (long long)h * (q.k + n));
+    return pr * Hkv * tcum[B] + Hkv * tcum[lo_b] + h * n + max(0, x - q.k);
+}
+// The CTA whose range holds tile T: the largest c with floor(c Wt / G) <= the weighted
+// start of T.
+__device__ __forceinline__ int cut_owner(const Cut& q, const int* tcum, int B, int Hkv, int W, int G, int T) {
+    if (q.k == 0) return int(((long long)(T + 1) * G - 1) / W);
+    int pr, b, h, j0, n;
+    unit_at(T, tcum, B, Hkv, pr, b, h, j0, n);
+    const long long ws = pr * q.WP + cut_wb(tcum, b, Hkv, q.k) + (long long)h * (q.k + n) + q.k + j0;
+    return int(((ws + 1) * G - 1) / q.Wt);
+}
 
 // Every role of a CTA walks the same ranges in the same order.  A range is named by the
 // global position of its first tile (persistent form; 0 for the single range of the other
@@ -228,10 +285,11 @@ __device__ __forceinline__ void write_piece(const AttnParams& p, uint32_t ocol, 
 // with the partials of the unit's other pieces (slot 2c of CTAs c0 + 1 .. c1: their first
 // ranges), once their flags are up, as splits merge: M = max m_k, l = sum l_k 2^(m_k - M),
 // O = sum O_k 2^(m_k - M); O / l leaves as bf16.  False if a flag did not come up in time.
-__device__ __forceinline__ bool merge_head(const AttnParams& p, uint32_t ocol, bool warp_rows, const Seg& s, int W,
-                                           int G, int t, int row, bool row_in, bool row_ok, int i, int hq, float m_own,
-                                           float l_own) {
-    const int c0 = st_owner(s.ub, W, G), c1 = st_owner(s.ue - 1, W, G);
+__device__ __forceinline__ bool merge_head(const AttnParams& p, uint32_t ocol, bool warp_rows, const Seg& s,
+                                           const int* tcum, int W, int G, int t, int row, bool row_in, bool row_ok,
+                                           int i, int hq, float m_own, float l_own) {
+    const Cut q = make_cut(tcum, p.B, p.Hkv, p.row_blocks / kNQ, G);
+    const int c0 = cut_owner(q, tcum, p.B, p.Hkv, W, G, s.ub), c1 = cut_owner(q, tcum, p.B, p.Hkv, W, G, s.ue - 1);
     bool ok = true;
     const uint64_t t_start = global_ns();
     for (int c = c0 + 1; c <= c1; ++c) {             // every piece's partial is in memory
@@ -334,8 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         walk.G = min(int(gridDim.x), walk.W);
         walk.lo = walk.hi = 0;
         if (walk.c < walk.G) {
-            walk.lo = st_lo(walk.c, walk.W, walk.G);
-            walk.hi = st_lo(walk.c + 1, walk.W, walk.G);
+            const Cut q = make_cut(tcum, p.B, p.Hkv, pairs, walk.G);
+            walk.lo = cut_lo(q, tcum, p.B, p.Hkv, walk.W, walk.G, walk.c);
+            walk.hi = cut_lo(q, tcum, p.B, p.Hkv, walk.W, walk.G, walk.c + 1);
         }
         // the units of invalid sequences are zeroed, each by one CTA
         for (int b = 0; b < p.B; ++b) {
@@ -691,7 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             walk.at(head_T, A);
             const RowOf ra = row_of(A);
             const bool wr = __any_sync(0xffffffffu, ra.ok);
-            alive = merge_head(p, ocol, wr, A, walk.W, walk.G, t, row, ra.in, ra.ok, ra.i, ra.hq, head_m, head_l);
+            alive = merge_head(p, ocol, wr, A, walk.tcum, walk.W, walk.G, t, row, ra.in, ra.ok, ra.i, ra.hq, head_m,
+                               head_l);
             tc_fence_before();
             mbar_arrive(&bars->o_free[t]);
         }
